@@ -1,0 +1,198 @@
+"""fp64 CPU oracle for blockwise packed attention and its chunk schedules.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the CPU baseline
+leg of the benchmark are the only callers. The product package never imports
+this module, and this module imports nothing from the product.
+
+The arithmetic lives in ``oracle.cpp`` (plain C++, double precision, OpenMP
+over rows); this file builds it with g++ and marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+DT_F64, DT_F32, DT_BF16 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with g++ (OpenMP) if it is missing or stale."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-fopenmp", "-fPIC", "-shared",
+                               _SRC, "-o", tmp])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        vp = ctypes.c_void_p
+        lib.oracle_attn.restype = ctypes.c_int
+        lib.oracle_attn.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_double, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                    f64p, f64p, ctypes.c_int]
+        lib.oracle_lse_merge.restype = None
+        lib.oracle_lse_merge.argtypes = [f64p, f64p, f64p, f64p, ctypes.c_longlong, ctypes.c_int,
+                                         f64p, f64p]
+        lib.oracle_valid_pairs.restype = ctypes.c_longlong
+        lib.oracle_valid_pairs.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_closed_form_schedule.restype = ctypes.c_longlong
+        lib.oracle_closed_form_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                                    ctypes.c_int, ctypes.c_int, i32p,
+                                                    ctypes.c_longlong]
+        lib.oracle_check_hamiltonian.restype = ctypes.c_int
+        lib.oracle_check_hamiltonian.argtypes = [ctypes.c_int, i32p]
+        lib.oracle_check_schedule.restype = ctypes.c_int
+        lib.oracle_check_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                              ctypes.c_int, ctypes.c_int, i32p, ctypes.c_longlong,
+                                              i32p, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
+        lib.oracle_check_cu_seqlens.restype = ctypes.c_int
+        lib.oracle_check_cu_seqlens.argtypes = [i32p, ctypes.c_int, ctypes.c_int]
+        lib.oracle_doc_of.restype = ctypes.c_int
+        lib.oracle_doc_of.argtypes = [i32p, ctypes.c_int, ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def _i32(a):
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _f64(a):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _as_input(x):
+    """Returns (contiguous array, dtype code). bf16 data is passed as uint16 bits."""
+    if x.dtype == np.float64:
+        return np.ascontiguousarray(x), DT_F64
+    if x.dtype == np.float32:
+        return np.ascontiguousarray(x), DT_F32
+    if x.dtype == np.uint16:
+        return np.ascontiguousarray(x), DT_BF16
+    raise TypeError(f"oracle input dtype {x.dtype} not supported")
+
+
+def attn(q, k, v, cu_seqlens, causal: bool, scale: float | None = None, rows=None,
+         kv_range=None, threads: int = 0):
+    """Exact attention in fp64.
+
+    q: [T, Hq, d]; k, v: [T, Hkv, d] (float64, float32, or uint16 bf16 bits).
+    rows: query tokens to evaluate (default all). kv_range: (kv_begin, kv_end).
+    Returns (o [n, Hq, d] float64, lse [n, Hq] float64), n = len(rows).
+    """
+    lib = _load()
+    q, dt = _as_input(q)
+    k, dk = _as_input(k)
+    v, dv = _as_input(v)
+    assert dt == dk == dv, "q, k, v must share a dtype"
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    assert k.shape == (T, Hkv, d) and v.shape == (T, Hkv, d)
+    cu, cup = _i32(cu_seqlens)
+    ndocs = len(cu) - 1
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if rows is None:
+        rows_arr, rowsp, n = None, None, T
+    else:
+        rows_arr, rowsp = _i32(rows)
+        n = len(rows_arr)
+    kb, ke = (0, T) if kv_range is None else kv_range
+    o = np.empty((n, Hq, d), dtype=np.float64)
+    lse = np.empty((n, Hq), dtype=np.float64)
+    rc = lib.oracle_attn(q.ctypes.data, k.ctypes.data, v.ctypes.data, dt, T, Hq, Hkv, d, cup,
+                         ndocs, int(causal), float(scale), int(kb), int(ke), rowsp, n,
+                         o.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                         lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn rejected its arguments (code {rc})")
+    return o, lse
+
+
+def lse_merge(o1, l1, o2, l2):
+    """Merge two normalised partials. o*: [..., d], l*: [...]. Returns (o, lse)."""
+    lib = _load()
+    d = o1.shape[-1]
+    n = int(np.prod(l1.shape))
+    o1c, o1p = _f64(o1)
+    o2c, o2p = _f64(o2)
+    l1c, l1p = _f64(l1)
+    l2c, l2p = _f64(l2)
+    o = np.empty(o1.shape, dtype=np.float64)
+    lo = np.empty(l1.shape, dtype=np.float64)
+    lib.oracle_lse_merge(o1p, l1p, o2p, l2p, n, d, o.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                         lo.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return o, lo
+
+
+def valid_pairs(cu_seqlens, causal: bool, qa: int, qb: int, ka: int, kb: int) -> int:
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    return int(lib.oracle_valid_pairs(cup, len(cu) - 1, int(causal), qa, qb, ka, kb))
+
+
+def doc_of(cu_seqlens, t: int) -> int:
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    return int(lib.oracle_doc_of(cup, len(cu) - 1, int(t)))
+
+
+def check_cu_seqlens(cu_seqlens, T: int) -> int:
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    return int(lib.oracle_check_cu_seqlens(cup, len(cu) - 1, int(T)))
+
+
+def closed_form_schedule(kind: int, P: int, T: int, cu_seqlens, causal: bool):
+    """Expected RING (0) / ZIGZAG (1) items [n, 8] (flags column left 0), or None."""
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    n = lib.oracle_closed_form_schedule(kind, P, T, cup, len(cu) - 1, int(causal), None, 0)
+    if n < 0:
+        return None
+    out = np.zeros((max(n, 1), 8), dtype=np.int32)
+    lib.oracle_closed_form_schedule(kind, P, T, cup, len(cu) - 1, int(causal),
+                                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n)
+    return out[:n]
+
+
+def check_hamiltonian(P: int, succ) -> int:
+    lib = _load()
+    s, sp = _i32(succ)
+    return int(lib.oracle_check_hamiltonian(P, sp))
+
+
+def check_schedule(kind: int, P: int, T: int, cu_seqlens, causal: bool, items, succ=None,
+                   brute: bool = False):
+    """Returns (code, message); code 0 means every property holds."""
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    it, itp = _i32(np.asarray(items).reshape(-1, 8))
+    if succ is None:
+        succ = np.zeros((max(P - 1, 1), max(P, 1)), dtype=np.int32)
+    sc, scp = _i32(succ)
+    buf = ctypes.create_string_buffer(256)
+    rc = lib.oracle_check_schedule(kind, P, T, cup, len(cu) - 1, int(causal), itp, len(it), scp,
+                                   int(brute), buf, 256)
+    return int(rc), buf.value.decode()

@@ -1,0 +1,419 @@
+// Plain fp64 CPU oracle for blockwise packed attention and its chunk schedules.
+//
+// TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the CPU
+// baseline leg of the benchmark may load this code. The product library never
+// links, includes or calls it, and this file includes nothing from the product.
+//
+// What it computes (sources):
+//  * Exact softmax attention restricted to each packed document, optionally
+//    causal. HSAP abstract ("correctly compute causal attention on the
+//    hybrid-context packed sequences"; packing causes "cross-contamination"),
+//    TASP abstract ("enable each Q tensor to access all KV tensors"). The
+//    formula is the textbook one: s_j = <q_i, k_j> * scale over the valid key
+//    set V(i) = { j : doc(j) == doc(i) and (not causal or j <= i) },
+//    LSE = log sum_j exp(s_j), O = sum_j exp(s_j - LSE) v_j.
+//  * GQA: query head h reads key/value head h / (Hq / Hkv) (GQA paper, cited in
+//    the TASP reference list).
+//  * Partials restricted to a key range [kv_begin, kv_end) and their
+//    log-sum-exp merge (the "partial attention computation" of the HSAP
+//    abstract; Blockwise/Ring Attention, cited by TASP).
+//  * Schedule properties: Ring AllGather visit order, zigzag chunking, and the
+//    Hamiltonian decomposition of the complete directed graph into orthogonal
+//    rings with the primitive decomposition of each chunk into P-1 pieces
+//    (TASP abstract).
+// Every floating-point step is in double precision; inputs may be given as
+// float64, float32 or bfloat16 bit patterns and are widened exactly.
+//
+// Parity pins for every function live in the CPU test suite (brute force,
+// closed forms, a library special case, merge and isolation invariants, and
+// hand-written schedule fixtures). No function here is unpinned.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cstdio>
+#include <vector>
+#include <algorithm>
+#include <limits>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+// Input dtype codes.
+enum { DT_F64 = 0, DT_F32 = 1, DT_BF16 = 2 };
+
+inline double widen(const void* base, int dtype, size_t idx) {
+  if (dtype == DT_F64) return static_cast<const double*>(base)[idx];
+  if (dtype == DT_F32) return static_cast<const float*>(base)[idx];
+  // bfloat16: the upper 16 bits of an IEEE float32.
+  uint32_t bits = static_cast<uint32_t>(static_cast<const uint16_t*>(base)[idx]) << 16;
+  float f;
+  std::memcpy(&f, &bits, sizeof f);
+  return f;
+}
+
+// Index of the document that holds token t: the i with cu[i] <= t < cu[i+1].
+int doc_of(const int32_t* cu, int ndocs, int t) {
+  int lo = 0, hi = ndocs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) / 2;
+    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+const double NEG_INF = -std::numeric_limits<double>::infinity();
+
+}  // namespace
+
+extern "C" {
+
+// Validates a cu_seqlens array: cu[0] == 0, strictly increasing, cu[ndocs] == T.
+// Returns 0 when valid.
+int oracle_check_cu_seqlens(const int32_t* cu, int ndocs, int T) {
+  if (ndocs < 1 || cu[0] != 0 || cu[ndocs] != T) return 1;
+  for (int i = 0; i < ndocs; ++i)
+    if (cu[i + 1] <= cu[i]) return 2;
+  return 0;
+}
+
+int oracle_doc_of(const int32_t* cu, int ndocs, int t) { return doc_of(cu, ndocs, t); }
+
+// Attention for the query tokens listed in `rows` (or every token when rows is
+// NULL and nrows == T), over the keys in [kv_begin, kv_end) that are valid for
+// that query. Layouts: q [T][Hq][d], k and v [T][Hkv][d]. Outputs:
+// o_out [nrows][Hq][d], lse_out [nrows][Hq]. A query with no valid key in the
+// range gets LSE = -inf and O = 0. Returns 0 on success.
+int oracle_attn(const void* q, const void* k, const void* v, int dtype,
+                int T, int Hq, int Hkv, int d,
+                const int32_t* cu, int ndocs, int causal, double scale,
+                int kv_begin, int kv_end,
+                const int32_t* rows, int nrows,
+                double* o_out, double* lse_out, int nthreads) {
+  if (T <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return 1;
+  if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return 2;
+  if (kv_begin < 0 || kv_end > T || kv_begin > kv_end) return 3;
+  const int G = Hq / Hkv;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  int bad_row = 0;
+#pragma omp parallel
+  {
+    std::vector<double> qi(d), s, acc(d);
+#pragma omp for schedule(dynamic, 1)
+    for (long long task = 0; task < static_cast<long long>(nrows) * Hq; ++task) {
+      const int r = static_cast<int>(task / Hq);
+      const int h = static_cast<int>(task % Hq);
+      const int i = rows ? rows[r] : r;
+      if (i < 0 || i >= T) { bad_row = 1; continue; }
+      const int g = h / G;
+      // V(i) restricted to [kv_begin, kv_end): the same document as i, and
+      // j <= i when causal. Documents are contiguous token ranges, so the set
+      // is one interval.
+      const int D = doc_of(cu, ndocs, i);
+      int j0 = std::max(cu[D], kv_begin);
+      int j1 = std::min(cu[D + 1], kv_end);
+      if (causal) j1 = std::min(j1, i + 1);
+      double* o_row = o_out + (static_cast<size_t>(r) * Hq + h) * d;
+      if (j1 <= j0) {
+        for (int c = 0; c < d; ++c) o_row[c] = 0.0;
+        lse_out[static_cast<size_t>(r) * Hq + h] = NEG_INF;
+        continue;
+      }
+      for (int c = 0; c < d; ++c) qi[c] = widen(q, dtype, (static_cast<size_t>(i) * Hq + h) * d + c);
+      s.resize(j1 - j0);
+      double m = NEG_INF;
+      for (int j = j0; j < j1; ++j) {
+        const size_t kb = (static_cast<size_t>(j) * Hkv + g) * d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += qi[c] * widen(k, dtype, kb + c);
+        s[j - j0] = dot * scale;
+        m = std::max(m, s[j - j0]);
+      }
+      double sum = 0.0;
+      for (int j = j0; j < j1; ++j) sum += std::exp(s[j - j0] - m);
+      const double lse = m + std::log(sum);
+      std::fill(acc.begin(), acc.end(), 0.0);
+      for (int j = j0; j < j1; ++j) {
+        const double w = std::exp(s[j - j0] - lse);
+        const size_t vb = (static_cast<size_t>(j) * Hkv + g) * d;
+        for (int c = 0; c < d; ++c) acc[c] += w * widen(v, dtype, vb + c);
+      }
+      for (int c = 0; c < d; ++c) o_row[c] = acc[c];
+      lse_out[static_cast<size_t>(r) * Hq + h] = lse;
+    }
+  }
+  return bad_row ? 4 : 0;
+}
+
+// Log-sum-exp merge of two normalised partials over disjoint key sets:
+//   L = M + log(exp(L1 - M) + exp(L2 - M)), M = max(L1, L2),
+//   O = exp(L1 - L) O1 + exp(L2 - L) O2.
+// A partial with L = -inf contributes nothing; two such stay -inf with O = 0.
+// Layouts: o [n][d], lse [n] (n = rows x heads, any order shared by all four).
+void oracle_lse_merge(const double* o1, const double* l1, const double* o2, const double* l2,
+                      long long n, int d, double* o_out, double* l_out) {
+  for (long long r = 0; r < n; ++r) {
+    const double a = l1[r], b = l2[r];
+    const double M = std::max(a, b);
+    if (M == NEG_INF) {
+      l_out[r] = NEG_INF;
+      for (int c = 0; c < d; ++c) o_out[r * d + c] = 0.0;
+      continue;
+    }
+    const double L = M + std::log(std::exp(a - M) + std::exp(b - M));
+    const double wa = std::exp(a - L), wb = std::exp(b - L);
+    for (int c = 0; c < d; ++c) o_out[r * d + c] = wa * o1[r * d + c] + wb * o2[r * d + c];
+    l_out[r] = L;
+  }
+}
+
+// Number of (query, key) pairs with query in [qa, qb) and key in [ka, kb)
+// that the document and causal masks allow. Brute force over documents.
+long long oracle_valid_pairs(const int32_t* cu, int ndocs, int causal,
+                             int qa, int qb, int ka, int kb) {
+  long long total = 0;
+  for (int D = 0; D < ndocs; ++D) {
+    const int r0 = std::max(qa, cu[D]), r1 = std::min(qb, cu[D + 1]);
+    const int c0 = std::max(ka, cu[D]), c1 = std::min(kb, cu[D + 1]);
+    if (r1 <= r0 || c1 <= c0) continue;
+    if (!causal) { total += static_cast<long long>(r1 - r0) * (c1 - c0); continue; }
+    for (int i = r0; i < r1; ++i) {
+      const int hi = std::min(c1, i + 1);
+      if (hi > c0) total += hi - c0;
+    }
+  }
+  return total;
+}
+
+// ---------------------------------------------------------------------------
+// Schedules.
+//
+// An item is 8 int32: rank, step, cycle, q_begin, q_end, kv_begin, kv_end,
+// flags. The checks below re-derive what the schedule must contain without
+// using the product's generator.
+
+// Bounds of piece `idx` when [0, n) is cut into `parts` contiguous pieces and
+// the first n mod parts pieces get one extra token.
+static void split_bounds(int n, int parts, int idx, int* b, int* e) {
+  const int base = n / parts, extra = n % parts;
+  *b = idx * base + std::min(idx, extra);
+  *e = *b + base + (idx < extra ? 1 : 0);
+}
+
+// Writes the expected RING (kind 0) or ZIGZAG (kind 1) item list, before and
+// after pruning of pairless items, in the canonical order: rank, then local Q
+// piece in token order, then step. Returns the number of items, or -1 when
+// the configuration is not allowed (zigzag needs T divisible by 2P).
+// `out` may be NULL to count only. Flags are not produced (written 0).
+long long oracle_closed_form_schedule(int kind, int P, int T, const int32_t* cu, int ndocs,
+                                      int causal, int32_t* out, long long cap) {
+  long long n = 0;
+  auto emit = [&](int r, int s, int qa, int qb, int ka, int kb) {
+    if (oracle_valid_pairs(cu, ndocs, causal, qa, qb, ka, kb) == 0) return;
+    if (out && n < cap) {
+      int32_t* it = out + n * 8;
+      it[0] = r; it[1] = s; it[2] = 0; it[3] = qa; it[4] = qb; it[5] = ka; it[6] = kb; it[7] = 0;
+    }
+    ++n;
+  };
+  if (kind == 0) {
+    for (int r = 0; r < P; ++r) {
+      int qa, qb;
+      split_bounds(T, P, r, &qa, &qb);
+      for (int s = 0; s < P; ++s) {
+        const int src = ((r - s) % P + P) % P;
+        int ka, kb;
+        split_bounds(T, P, src, &ka, &kb);
+        emit(r, s, qa, qb, ka, kb);
+      }
+    }
+    return n;
+  }
+  if (kind == 1) {
+    if (T % (2 * P) != 0) return -1;
+    const int c = T / (2 * P);
+    for (int r = 0; r < P; ++r) {
+      const int mine[2] = {r, 2 * P - 1 - r};  // r < 2P-1-r, so token order
+      for (int a = 0; a < 2; ++a) {
+        for (int s = 0; s < P; ++s) {
+          const int src = ((r - s) % P + P) % P;
+          const int theirs[2] = {src, 2 * P - 1 - src};
+          for (int b = 0; b < 2; ++b)
+            emit(r, s, mine[a] * c, (mine[a] + 1) * c, theirs[b] * c, (theirs[b] + 1) * c);
+        }
+      }
+    }
+    return n;
+  }
+  return -1;
+}
+
+// Checks that succ (P-1 rows of P successors) is a decomposition of the
+// complete directed graph on P vertices into P-1 arc-disjoint directed
+// Hamiltonian cycles. Returns 0 when it is; otherwise a nonzero code:
+// 1 bad vertex id or self loop, 2 a row is not one P-cycle, 3 an arc repeats.
+int oracle_check_hamiltonian(int P, const int32_t* succ) {
+  if (P < 2) return 0;
+  std::vector<int> used(static_cast<size_t>(P) * P, 0);
+  for (int c = 0; c < P - 1; ++c) {
+    const int32_t* sc = succ + static_cast<size_t>(c) * P;
+    for (int u = 0; u < P; ++u)
+      if (sc[u] < 0 || sc[u] >= P || sc[u] == u) return 1;
+    // Walk from 0: a Hamiltonian cycle returns to 0 after exactly P arcs and
+    // visits every vertex once.
+    std::vector<int> seen(P, 0);
+    int u = 0;
+    for (int step = 0; step < P; ++step) {
+      if (seen[u]) return 2;
+      seen[u] = 1;
+      u = sc[u];
+    }
+    if (u != 0) return 2;
+    for (int w = 0; w < P; ++w) {
+      int& cnt = used[static_cast<size_t>(w) * P + sc[w]];
+      if (++cnt > 1) return 3;
+    }
+  }
+  // P-1 cycles of P arcs, none repeated, no self loops: all P(P-1) arcs used.
+  return 0;
+}
+
+// Checks an item list against the method's requirements. Returns 0 when all
+// hold, else a code, and writes a one-line reason into msg.
+//   * every item lies inside [0, T), has begin < end and at least one valid
+//     (query, key) pair (the sequence-aware pruning: no item without work);
+//   * the Q ranges: rank r of RING/TASP owns chunk r of P; rank r of ZIGZAG
+//     owns chunks r and 2P-1-r of 2P;
+//   * for each rank and each of its Q ranges, the item key ranges are pairwise
+//     disjoint, and together they contain every key that some query of the
+//     range may attend (so each valid pair is computed exactly once);
+//   * TASP (kind 2): step 0 is the local chunk; at step t >= 1 the item of
+//     cycle c holds piece c of chunk pred_c^t(r), where pred_c inverts row c
+//     of succ and piece c is cut by the "first n mod (P-1) pieces get one
+//     more token" rule; succ must pass oracle_check_hamiltonian.
+// If brute is nonzero, the exact-once property is additionally checked by
+// counting every valid pair (use only for small T).
+int oracle_check_schedule(int kind, int P, int T, const int32_t* cu, int ndocs, int causal,
+                          const int32_t* items, long long n_items, const int32_t* succ,
+                          int brute, char* msg, int msg_len) {
+  auto fail = [&](int code, const char* fmt, long long a, long long b) {
+    if (msg && msg_len > 0) std::snprintf(msg, msg_len, fmt, a, b);
+    return code;
+  };
+  if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return fail(1, "bad cu_seqlens %lld %lld", 0, 0);
+  if (P < 1) return fail(1, "bad P %lld %lld", P, 0);
+  // Owned Q ranges per rank.
+  std::vector<std::vector<std::pair<int, int>>> own(P);
+  for (int r = 0; r < P; ++r) {
+    if (kind == 1) {
+      if (T % (2 * P) != 0) return fail(1, "zigzag needs T %% 2P == 0 (T=%lld, P=%lld)", T, P);
+      const int c = T / (2 * P);
+      own[r].push_back({r * c, (r + 1) * c});
+      own[r].push_back({(2 * P - 1 - r) * c, (2 * P - r) * c});
+    } else {
+      int a, b;
+      split_bounds(T, P, r, &a, &b);
+      own[r].push_back({a, b});
+    }
+  }
+  if (kind == 2 && P >= 2) {
+    const int hc = oracle_check_hamiltonian(P, succ);
+    if (hc != 0) return fail(2, "not a Hamiltonian decomposition (code %lld) %lld", hc, 0);
+  }
+  // pred tables for TASP.
+  std::vector<int> pred;
+  if (kind == 2 && P >= 2) {
+    pred.assign(static_cast<size_t>(P - 1) * P, -1);
+    for (int c = 0; c < P - 1; ++c)
+      for (int u = 0; u < P; ++u) pred[static_cast<size_t>(c) * P + succ[static_cast<size_t>(c) * P + u]] = u;
+  }
+  // Per (rank, q range): list of key ranges.
+  std::vector<std::vector<std::vector<std::pair<int, int>>>> keys(P);
+  for (int r = 0; r < P; ++r) keys[r].resize(own[r].size());
+  for (long long x = 0; x < n_items; ++x) {
+    const int32_t* it = items + x * 8;
+    const int r = it[0], s = it[1], c = it[2], qa = it[3], qb = it[4], ka = it[5], kb = it[6];
+    if (r < 0 || r >= P) return fail(3, "item %lld: bad rank %lld", x, r);
+    if (!(0 <= qa && qa < qb && qb <= T && 0 <= ka && ka < kb && kb <= T))
+      return fail(3, "item %lld: bad ranges (q_begin %lld)", x, qa);
+    if (oracle_valid_pairs(cu, ndocs, causal, qa, qb, ka, kb) == 0)
+      return fail(4, "item %lld has no valid pair (rank %lld)", x, r);
+    int which = -1;
+    for (size_t w = 0; w < own[r].size(); ++w)
+      if (own[r][w].first == qa && own[r][w].second == qb) which = static_cast<int>(w);
+    if (which < 0) return fail(5, "item %lld: Q range not owned by rank %lld", x, r);
+    keys[r][which].push_back({ka, kb});
+    if (kind == 2) {
+      int ea, eb;
+      if (s == 0) {
+        split_bounds(T, P, r, &ea, &eb);
+      } else {
+        if (P < 2 || c < 0 || c >= P - 1 || s >= P) return fail(6, "item %lld: bad step/cycle %lld", x, s);
+        int src = r;
+        for (int t = 0; t < s; ++t) src = pred[static_cast<size_t>(c) * P + src];
+        int cb, ce;
+        split_bounds(T, P, src, &cb, &ce);
+        int pb, pe;
+        split_bounds(ce - cb, P - 1, c, &pb, &pe);
+        ea = cb + pb;
+        eb = cb + pe;
+      }
+      if (ka != ea || kb != eb) return fail(7, "item %lld: TASP key range starts %lld, expected", x, ka);
+    }
+  }
+  // Coverage: disjoint and complete for each owned Q range.
+  for (int r = 0; r < P; ++r) {
+    for (size_t w = 0; w < own[r].size(); ++w) {
+      auto ks = keys[r][w];
+      std::sort(ks.begin(), ks.end());
+      for (size_t y = 1; y < ks.size(); ++y)
+        if (ks[y].first < ks[y - 1].second) return fail(8, "rank %lld: overlapping key ranges at %lld", r, ks[y].first);
+      const int qa = own[r][w].first, qb = own[r][w].second;
+      // Keys some query of [qa, qb) may attend: per document D meeting the
+      // range, [cu[D], cu[D+1]) (non-causal) or [cu[D], min(cu[D+1], qb)).
+      for (int D = 0; D < ndocs; ++D) {
+        if (cu[D + 1] <= qa || cu[D] >= qb) continue;
+        const int need0 = cu[D];
+        const int need1 = causal ? std::min(cu[D + 1], qb) : cu[D + 1];
+        // Walk the sorted disjoint ranges and make sure [need0, need1) is covered.
+        int pos = need0;
+        for (const auto& kr : ks) {
+          if (kr.second <= pos) continue;
+          if (kr.first > pos) break;
+          pos = kr.second;
+          if (pos >= need1) break;
+        }
+        if (pos < need1) return fail(9, "rank %lld: key %lld needed but not covered", r, pos);
+      }
+    }
+  }
+  if (brute) {
+    std::vector<int> doc(T);
+    for (int t = 0; t < T; ++t) doc[t] = doc_of(cu, ndocs, t);
+    std::vector<uint8_t> cnt(static_cast<size_t>(T) * T, 0);
+    for (long long x = 0; x < n_items; ++x) {
+      const int32_t* it = items + x * 8;
+      for (int i = it[3]; i < it[4]; ++i)
+        for (int j = it[5]; j < it[6]; ++j) {
+          if (doc[i] != doc[j] || (causal && j > i)) continue;
+          uint8_t& cc = cnt[static_cast<size_t>(i) * T + j];
+          if (cc < 255) ++cc;
+        }
+    }
+    for (int i = 0; i < T; ++i)
+      for (int j = 0; j < T; ++j) {
+        const bool valid = (doc[i] == doc[j]) && (!causal || j <= i);
+        const uint8_t cc = cnt[static_cast<size_t>(i) * T + j];
+        if (valid && cc != 1) return fail(10, "pair (%lld, %lld) not computed exactly once", i, j);
+      }
+  }
+  return 0;
+}
+
+}  // extern "C"
