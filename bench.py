@@ -1,0 +1,394 @@
+"""Throughput of packed blockwise attention on GB300, as one JSON line.
+
+A step is one sp_packed_attention call (set-up kernel + persistent attention
+kernel) over the whole chunk schedule of the benchmark workload: the Llama-style
+GQA layer (32 query / 8 key-value heads, d = 128, 32K tokens in one document,
+causal, 8 virtual ranks in zigzag order), bf16 inputs resident in HBM.
+FLOP = 4 * d * Hq * (valid query-key pairs).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own copy of the workload (independent
+problems, no collective on the data path: weak scaling); the timed region is
+bracketed by a barrier and device synchronisation, and its maximum over ranks
+is reported. `--impl reference` times the fp64 CPU oracle on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed causal attention TFLOP/s (valid pairs) on 1 GB300 and % of bf16 peak"
+L2_BYTES = 129 * 1024 * 1024
+WORKLOAD_INDEX = 1  # the Llama-style layer the metric is quoted on
+
+
+def valid_pairs(cu, causal: bool) -> int:
+    lens = np.diff(np.asarray(cu, dtype=np.int64))
+    if causal:
+        return int(np.sum(lens * (lens + 1) // 2))
+    return int(np.sum(lens * lens))
+
+
+def sched_name(kind: int) -> str:
+    return {0: "ring", 1: "zigzag", 2: "tasp"}[kind]
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]), "hbm_gbs": float(p["hbm_gbs"]),
+                "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_traffic():
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "attn_tc_traffic.json")
+    src = os.path.join(ROOT, "sequence_blockwise_gb300", "csrc", "attn_tc.cu")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("attn_tc_cu_sha256") == sha:
+            return float(rec["traffic_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, cu, seconds: float, seed: int = 0):
+    """Runs the fp64 oracle on random query rows of workload w (all heads),
+    growing the sample until it has run for about `seconds`. Inputs are drawn
+    on the CPU with the workload's generator for the keys the rows need.
+    Returns (flop, elapsed_s, n_rows, threads)."""
+    import torch
+    import oracle
+    from sequence_blockwise_gb300 import workloads as wl
+    rng = np.random.default_rng(seed)
+    oracle.build()
+    # Inputs: the same seeded recipe on the CPU.
+    q, k, v = wl.make_qkv(w, "cpu")
+    conv = (lambda t: wl.bf16_bits(t)) if w.dtype == "bf16" else (lambda t: t.numpy())
+    kh, vh = conv(k), conv(v)
+    threads = os.cpu_count() or 1
+    flop, elapsed, nrows = 0, 0.0, 0
+    batch = 16
+    while elapsed < seconds:
+        rows = np.sort(rng.integers(0, w.T, size=batch)).astype(np.int32)
+        qr = conv(q[torch.from_numpy(rows.astype(np.int64))])
+        lens = np.diff(cu)
+        doc = np.searchsorted(cu, rows, side="right") - 1
+        keys = (rows - cu[doc] + 1) if w.causal else lens[doc]
+        t0 = time.perf_counter()
+        oracle.attn(qr, kh, vh, cu, w.causal, rows=rows, q_rows_only=True, threads=threads)
+        elapsed += time.perf_counter() - t0
+        flop += int(4 * w.d * w.Hq * int(np.sum(keys)))
+        nrows += batch
+        batch = min(batch * 2, 1024)
+    return flop, elapsed, nrows, threads
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, world, rank, local):
+    import torch
+    import sequence_blockwise_gb300 as sb
+    from sequence_blockwise_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[WORKLOAD_INDEX]
+    cu = wl.cu_seqlens(w)
+    pairs = valid_pairs(cu, w.causal)
+    flop = 4.0 * w.d * w.Hq * pairs
+    dev = torch.device("cuda", local)
+    q, k, v = wl.make_qkv(w, dev)
+    att = sb.PackedAttention(cu, w.causal, w.kind, w.P, w.Hq, seed=w.seed, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 2  # set-up kernel + persistent attention kernel
+
+    def step():
+        att(q, k, v, o, lse, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    sb.sp_check_device_status(stream)
+
+    # ---- device-resident timed region
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier(world)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    per = [a.elapsed_time(b) for a, b in ev]
+    sb.sp_check_device_status(stream)
+    total_ms = dist_max(total_ms, world)
+    ms_step = total_ms / args.steps
+    value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C-ABI with host buffers
+    qh = q.cpu().pin_memory()
+    kh = k.cpu().pin_memory()
+    vh = v.cpu().pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    cu_h = torch.from_numpy(cu).pin_memory()
+    it_h = torch.from_numpy(att.items).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    h2d = (qh.numel() * qh.element_size() + kh.numel() * kh.element_size() +
+           vh.numel() * vh.element_size() + cu_h.numel() * 4 + it_h.numel() * 4)
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        att.cu_dev.copy_(cu_h, non_blocking=True)
+        att.items_dev.copy_(it_h, non_blocking=True)
+        sb.sp_packed_attention(qd, kd, vd, o, lse, att.cu_dev, w.causal, att.items_dev,
+                               att.workspace, stream=stream)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier(world)
+    e2e_ms = dist_max(e0.elapsed_time(e1), world)
+    e2e_value = world * flop * args.steps / (e2e_ms * 1e-3) / 1e12
+    sb.sp_check_device_status(stream)
+
+    peaks = read_peaks()
+    avg_launch_ms = sum(per) / len(per)
+    achieved = flop / (avg_launch_ms * 1e-3) / 1e12
+    traffic = kernel_traffic()
+    io_bytes = (q.numel() + k.numel() + v.numel() + o.numel()) * 2 + lse.numel() * 4
+
+    result = None
+    if rank == 0:
+        result = {
+            "metric": METRIC,
+            "value": round(value, 3),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) Q/K/V rounded to bf16; no dataset or weights)",
+            "config": {
+                "workload": w.name, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                "causal": w.causal, "docs": int(len(cu) - 1), "schedule": sched_name(w.kind),
+                "P_virtual": w.P, "n_items": int(len(att.items)), "valid_pairs": pairs,
+                "flop_per_step": flop, "parallelism": f"weak x{world} (independent problems)",
+                "l2": f"inputs+outputs {io_bytes / 2**20:.0f} MiB > L2 129 MiB; no flush",
+            },
+            "pct_of_peak": round(100.0 * value / world / peaks["bf16_tflops"], 2),
+            "roofline": {
+                "bound": "tensor", "achieved": round(achieved, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                "traffic": traffic,
+                "kernel": "attn_tc_kernel<128,0> (+ prep_kernel inside the timed call)",
+                "avg_launch_ms": round(avg_launch_ms, 4),
+            },
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+    return result, w, cu
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline field")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world, rank, local = dist_setup()
+    from sequence_blockwise_gb300 import workloads as wl
+    w = wl.WORKLOADS[WORKLOAD_INDEX]
+    cu = wl.cu_seqlens(w)
+
+    if args.impl == "reference":
+        # The fp64 CPU oracle on a bounded sample per step, rank 0 only.
+        if rank == 0:
+            per_step = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+            for _ in range(args.warmup):
+                oracle_sample(w, cu, per_step * 0.25, seed=99)
+            flop = elapsed = rows = 0
+            threads = 1
+            for s in range(args.steps):
+                f, e, n, threads = oracle_sample(w, cu, per_step, seed=s)
+                flop, elapsed, rows = flop + f, elapsed + e, rows + n
+            value = flop / elapsed / 1e12
+            sample = (f"{rows} random query rows x {w.Hq} heads over {args.steps} steps "
+                      f"(~{per_step:.0f} s each) of {w.name}")
+            print(json.dumps({
+                "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000.0 * elapsed / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "schedule": sched_name(w.kind), "P_virtual": w.P},
+                "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "gpu_launches": 0,
+            }), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    result, w, cu = run_ours(args, world, rank, local)
+    if rank == 0:
+        if args.no_cpu_baseline or world > 1:
+            result["cpu_baseline"] = None
+        else:
+            f, e, n, threads = oracle_sample(w, cu, args.cpu_seconds)
+            result["cpu_baseline"] = {
+                "value": round(f / e / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+                "kind": "oracle",
+                "sample": f"{n} random query rows x {w.Hq} heads of {w.name}, fp64, {e:.1f} s",
+            }
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

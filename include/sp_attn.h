@@ -1,0 +1,182 @@
+/*
+ * libsp_attn: the per-device hot path of sequence-parallel attention
+ * (Ring / Zigzag-Ring / TASP / HSAP) on one GB300, with the P sequence-parallel
+ * ranks virtual.
+ *
+ * Sources for what is computed:
+ *  - "TASP: Topology-aware Sequence Parallelism", abstract: Ring Attention
+ *    splits the query into chunks, and every Q chunk must reach every KV chunk
+ *    through the iterations of a Ring AllGather; TASP decomposes the complete
+ *    directed graph of ranks into orthogonal (arc-disjoint) Hamiltonian rings
+ *    and the AllGather of every iteration into the same number of concurrent
+ *    ring transfers.
+ *  - "HSAP: A Hierarchical Sequence-aware Parallelism for Hybrid-Context
+ *    Generative Models", abstract: attention on hybrid-context packed
+ *    sequences must be causal and must not cross documents; the computation
+ *    is a sequence of partial attention steps driven by per-device
+ *    instruction sequences generated ahead of time.
+ *
+ * Conventions shared by every call:
+ *  - T packed tokens, Hq query heads, Hkv key/value heads (Hq % Hkv == 0;
+ *    query head h reads key/value head h / (Hq / Hkv)), head dim d.
+ *  - Q and O: [T][Hq][d] row-major; K and V: [T][Hkv][d] row-major.
+ *    LSE of a full result: [Hq][T] float32, natural log.
+ *  - cu_seqlens: int32 [ndocs + 1], cu[0] = 0, strictly increasing,
+ *    cu[ndocs] = T. Document i is the token range [cu[i], cu[i+1]).
+ *  - Mask: query i may attend key j iff both lie in the same document and,
+ *    when causal, j <= i.
+ *  - Softmax scale: `scale` multiplies q.k (pass 1/sqrt(d) for the usual one).
+ *  - Ownership: the caller allocates and frees every buffer; the library keeps
+ *    no pointer after a call returns and allocates no device memory.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).
+ *    Device work is asynchronous on it. Argument errors are returned before
+ *    any launch. Device-side failures (a bounded wait that ran out, an item
+ *    that is out of range) set a per-device error word that
+ *    sp_check_device_status() reads.
+ *  - Alignment: every device pointer must be 16-byte aligned.
+ */
+#ifndef SP_ATTN_H
+#define SP_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SP_OK = 0,
+  SP_ERR_INVALID_ARG = 1,      /* a NULL pointer, a bad size, bad cu_seqlens, a misaligned pointer */
+  SP_ERR_UNSUPPORTED = 2,      /* valid but not implemented here (e.g. d not 64/128, TASP with P in {4,6}) */
+  SP_ERR_BUFFER_TOO_SMALL = 3, /* output count or workspace smaller than needed */
+  SP_ERR_CUDA = 4,             /* a CUDA runtime call failed */
+  SP_ERR_TIMEOUT = 5,          /* a device-side bounded wait ran out */
+  SP_ERR_INTERNAL = 6          /* a device-side consistency check failed */
+} sp_status;
+
+typedef enum { SP_SCHED_RING = 0, SP_SCHED_ZIGZAG = 1, SP_SCHED_TASP = 2 } sp_sched_kind;
+
+typedef enum { SP_DTYPE_BF16 = 0, SP_DTYPE_FP32 = 1 } sp_dtype;
+
+/* One step of one virtual rank: the Q rows [q_begin, q_end) of `rank` attend
+ * the keys [kv_begin, kv_end) that reached it at `step` (over Hamiltonian
+ * ring `cycle` for TASP; 0 otherwise). 32 bytes, all int32. */
+typedef struct {
+  int32_t rank, step, cycle, q_begin, q_end, kv_begin, kv_end, flags;
+} sp_item;
+
+#define SP_ITEM_CAUSAL_EDGE 1 /* flags bit: some pair of the item is masked by causality */
+#define SP_ITEM_DOC_EDGE 2    /* flags bit: some pair of the item is masked by a document boundary */
+
+/* sp_schedule_build — host only; builds the chunk-visit schedule ("device
+ * instruction sequence", HSAP abstract) of every virtual rank.
+ *
+ *  kind RING:   [0,T) cut into P contiguous chunks (the first T mod P get one
+ *               extra token); rank r owns chunk r; at step s it holds the KV
+ *               chunk of rank (r - s) mod P (TASP abstract, Ring AllGather).
+ *  kind ZIGZAG: 2P equal chunks (T % 2P must be 0); rank r owns chunks r and
+ *               2P-1-r; at step s it holds both chunks of rank (r - s) mod P.
+ *               One item per (own chunk, held chunk) pair.
+ *  kind TASP:   P chunks as RING. P-1 arc-disjoint directed Hamiltonian
+ *               cycles of the complete digraph on P ranks (deterministic in
+ *               `seed`, see sp_tasp_cycles); every KV chunk is cut into P-1
+ *               contiguous pieces (the first n mod (P-1) get one extra token).
+ *               Step 0 is the local chunk; at step t >= 1 ring c brings piece
+ *               c of the chunk of the rank t hops upstream on ring c (TASP
+ *               abstract: topology decomposition and primitive decomposition).
+ *               P in {4, 6} has no such decomposition: SP_ERR_UNSUPPORTED.
+ *               P <= 64.
+ *  Sequence-aware pruning (HSAP abstract): items without a single valid
+ *  (query, key) pair under the document and causal masks are left out.
+ *  Order: by rank, then the rank's Q ranges in token order, then step, then
+ *  cycle (TASP) or the held chunks in token order (ZIGZAG). Items that share
+ *  a rank and Q range are therefore contiguous, which sp_packed_attention
+ *  requires.
+ *
+ *  cu_seqlens_host: host int32 [ndocs + 1]. Two-call protocol: with
+ *  out_items == NULL only the count is written to *inout_n_items; otherwise
+ *  *inout_n_items is the capacity on input (SP_ERR_BUFFER_TOO_SMALL if short,
+ *  with the needed count written back) and the count on output. */
+sp_status sp_schedule_build(sp_sched_kind kind, int32_t P, int32_t total_tokens,
+                            const int32_t* cu_seqlens_host, int32_t ndocs, int32_t causal,
+                            uint64_t seed, sp_item* out_items, int64_t* inout_n_items);
+
+/* sp_tasp_cycles — host only. Writes the P-1 Hamiltonian cycles that TASP
+ * schedules use for (P, seed) as successor tables: out_succ[c * P + u] is the
+ * rank after u on ring c. out_succ must hold (P-1)*P int32. P = 1 writes
+ * nothing. Same errors as the TASP schedule. Results are cached per (P, seed). */
+sp_status sp_tasp_cycles(int32_t P, uint64_t seed, int32_t* out_succ);
+
+/* sp_partial_attn — one partial attention step ("partial attention
+ * computation", HSAP abstract; one iteration of Ring Attention, TASP abstract).
+ * For every query row t in [q_begin, q_end) and head h, over the keys
+ * j in [kv_begin, kv_end) that the mask allows:
+ *   lse_part[h][t - q_begin] = log sum_j exp(scale * q_t.k_j)
+ *   o_part[t - q_begin][h][:] = sum_j exp(scale * q_t.k_j - lse) v_j
+ * A row with no allowed key gets lse = -inf and o = 0.
+ *  q, k, v: device, dtype as given (bf16 runs on the tensor cores; fp32 runs on
+ *           CUDA cores in fp32 for the 1e-5 tolerance).
+ *  o_part: device float32 [q_end - q_begin][Hq][d]; lse_part: device float32
+ *          [Hq][q_end - q_begin].
+ *  cu_seqlens_dev: device int32 [ndocs + 1] (validity is the caller's duty).
+ *  d must be 64 or 128. An empty row range is a no-op. */
+sp_status sp_partial_attn(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                          int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,
+                          int32_t q_begin, int32_t q_end, int32_t kv_begin, int32_t kv_end,
+                          const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal, float scale,
+                          void* stream);
+
+/* sp_lse_merge — folds one normalised partial into an accumulator, in place,
+ * by the log-sum-exp rule (exact for partials over disjoint key sets):
+ *   M = max(L1, L2), L = M + log(exp(L1 - M) + exp(L2 - M)),
+ *   O = exp(L1 - L) O1 + exp(L2 - L) O2.
+ * A partial with L = -inf is the identity; two -inf stay -inf with O = 0.
+ *  o_acc, o_part: device float32 [rows][Hq][d]; lse_acc, lse_part: device
+ *  float32 [Hq][rows]. d % 4 == 0. Bandwidth bound: 12 bytes per O element. */
+sp_status sp_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+                       int32_t rows, int32_t Hq, int32_t d, void* stream);
+
+/* Bytes of device workspace sp_packed_attention needs for n_items items. */
+size_t sp_packed_attention_workspace_size(int64_t n_items);
+
+/* sp_packed_attention — the whole schedule in one persistent launch (plus a
+ * small set-up kernel): for every query row, the items of its rank and Q range
+ * are visited in schedule order and their partials are merged on chip with
+ * the log-sum-exp rule, so the result is exact masked attention over each
+ * packed document (HSAP abstract; TASP abstract).
+ *  o: device [T][Hq][d] in `dtype` (bf16 rounded to nearest even); lse: device
+ *     float32 [Hq][T], natural log.
+ *  items_dev: device copy of a schedule from sp_schedule_build (or any item
+ *     list whose Q ranges do not overlap across groups and whose items with
+ *     the same rank and Q range are contiguous); rows of [0, T) covered by no
+ *     item are not written.
+ *  workspace: device, at least sp_packed_attention_workspace_size(n_items)
+ *     bytes, owned by the caller, reused between calls; calls that share a
+ *     workspace must not overlap in time.
+ *  An inconsistent item list is reported through sp_check_device_status. */
+sp_status sp_packed_attention(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,
+                              const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal, float scale,
+                              const sp_item* items_dev, int64_t n_items, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the current device's error word, and
+ * returns SP_OK, SP_ERR_TIMEOUT, SP_ERR_INTERNAL, or SP_ERR_CUDA when the
+ * stream itself reports a CUDA error. */
+sp_status sp_check_device_status(void* stream);
+
+/* Diagnostic: launches one block whose thread waits on a barrier that nothing
+ * completes, bounded by timeout_ns of GPU time; the wait gives up, records
+ * SP_ERR_TIMEOUT in the error word and the block exits normally. Checks that
+ * bounded waits end and report. */
+sp_status sp_selftest_bounded_wait(uint64_t timeout_ns, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* sp_status_string(sp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SP_ATTN_H */

@@ -47,7 +47,7 @@ def _load():
         lib.oracle_attn.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_double, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
-                                    f64p, f64p, ctypes.c_int]
+                                    ctypes.c_int, f64p, f64p, ctypes.c_int]
         lib.oracle_lse_merge.restype = None
         lib.oracle_lse_merge.argtypes = [f64p, f64p, f64p, f64p, ctypes.c_longlong, ctypes.c_int,
                                          f64p, f64p]
@@ -94,11 +94,12 @@ def _as_input(x):
 
 
 def attn(q, k, v, cu_seqlens, causal: bool, scale: float | None = None, rows=None,
-         kv_range=None, threads: int = 0):
+         kv_range=None, threads: int = 0, q_rows_only: bool = False):
     """Exact attention in fp64.
 
-    q: [T, Hq, d]; k, v: [T, Hkv, d] (float64, float32, or uint16 bf16 bits).
-    rows: query tokens to evaluate (default all). kv_range: (kv_begin, kv_end).
+    q: [T, Hq, d] (or [len(rows), Hq, d] with q_rows_only); k, v: [T, Hkv, d]
+    (float64, float32, or uint16 bf16 bits). rows: query tokens to evaluate
+    (default all). kv_range: (kv_begin, kv_end).
     Returns (o [n, Hq, d] float64, lse [n, Hq] float64), n = len(rows).
     """
     lib = _load()
@@ -106,24 +107,27 @@ def attn(q, k, v, cu_seqlens, causal: bool, scale: float | None = None, rows=Non
     k, dk = _as_input(k)
     v, dv = _as_input(v)
     assert dt == dk == dv, "q, k, v must share a dtype"
-    T, Hq, d = q.shape
-    Hkv = k.shape[1]
+    _, Hq, d = q.shape
+    T, Hkv = k.shape[0], k.shape[1]
     assert k.shape == (T, Hkv, d) and v.shape == (T, Hkv, d)
+    assert q_rows_only or q.shape[0] == T
     cu, cup = _i32(cu_seqlens)
     ndocs = len(cu) - 1
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     if rows is None:
+        assert not q_rows_only
         rows_arr, rowsp, n = None, None, T
     else:
         rows_arr, rowsp = _i32(rows)
         n = len(rows_arr)
+        assert not q_rows_only or q.shape[0] == n
     kb, ke = (0, T) if kv_range is None else kv_range
     o = np.empty((n, Hq, d), dtype=np.float64)
     lse = np.empty((n, Hq), dtype=np.float64)
     rc = lib.oracle_attn(q.ctypes.data, k.ctypes.data, v.ctypes.data, dt, T, Hq, Hkv, d, cup,
                          ndocs, int(causal), float(scale), int(kb), int(ke), rowsp, n,
-                         o.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                         int(q_rows_only), o.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                          lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attn rejected its arguments (code {rc})")

@@ -83,14 +83,15 @@ int oracle_doc_of(const int32_t* cu, int ndocs, int t) { return doc_of(cu, ndocs
 
 // Attention for the query tokens listed in `rows` (or every token when rows is
 // NULL and nrows == T), over the keys in [kv_begin, kv_end) that are valid for
-// that query. Layouts: q [T][Hq][d], k and v [T][Hkv][d]. Outputs:
+// that query. Layouts: q [T][Hq][d] (or [nrows][Hq][d] holding only the listed
+// rows when q_rows_only is set), k and v [T][Hkv][d]. Outputs:
 // o_out [nrows][Hq][d], lse_out [nrows][Hq]. A query with no valid key in the
 // range gets LSE = -inf and O = 0. Returns 0 on success.
 int oracle_attn(const void* q, const void* k, const void* v, int dtype,
                 int T, int Hq, int Hkv, int d,
                 const int32_t* cu, int ndocs, int causal, double scale,
                 int kv_begin, int kv_end,
-                const int32_t* rows, int nrows,
+                const int32_t* rows, int nrows, int q_rows_only,
                 double* o_out, double* lse_out, int nthreads) {
   if (T <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return 1;
   if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return 2;
@@ -125,7 +126,8 @@ int oracle_attn(const void* q, const void* k, const void* v, int dtype,
         lse_out[static_cast<size_t>(r) * Hq + h] = NEG_INF;
         continue;
       }
-      for (int c = 0; c < d; ++c) qi[c] = widen(q, dtype, (static_cast<size_t>(i) * Hq + h) * d + c);
+      const size_t qrow = q_rows_only ? static_cast<size_t>(r) : static_cast<size_t>(i);
+      for (int c = 0; c < d; ++c) qi[c] = widen(q, dtype, (qrow * Hq + h) * d + c);
       s.resize(j1 - j0);
       double m = NEG_INF;
       for (int j = j0; j < j1; ++j) {

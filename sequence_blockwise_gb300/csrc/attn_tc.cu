@@ -1,0 +1,528 @@
+// Blockwise packed attention on the 5th-generation tensor cores (sm_103a).
+//
+// One persistent CTA per SM walks work units (group, 256 query rows, query
+// head). For each unit it visits the group's items in schedule order and each
+// item's keys in 128-key tiles; every tile is one "partial attention" step
+// (HSAP abstract) whose partial (O, LSE) is merged on chip into the running
+// state by the log-sum-exp rule, the merge Ring Attention applies between
+// ring steps (TASP abstract). Masks: same document, and key <= query when
+// causal (HSAP abstract: no cross-contamination of packed documents).
+//
+// Roles (12 warps):
+//   warp 0      TMA producer: Q tiles once per unit, K and V tiles into a
+//               2-stage ring (128-byte swizzled, as the MMA reads them).
+//   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma.
+//   warps 4-7   softmax for Q tile 0 (rows 0-127 of the unit).
+//   warps 8-11  softmax for Q tile 1 (rows 128-255).
+// Tensor memory (512 columns): S_i at column 128*i (fp32 128x128), the bf16
+// probabilities P_i written back over columns [64,128) of S_i, and the output
+// accumulators O_i at 256 + D*i.
+// Per KV tile j the MMA order is QK0(j), PV1(j-1), QK1(j), PV0(j): each
+// softmax warpgroup has two tensor-core steps of slack, and because MMAs from
+// one thread execute in order, the completion of QK_i(j) also implies that
+// PV_i(j-1) is done, so the softmax may rescale O_i without another wait.
+// The running maximum is only moved when it grows by more than 2^8, so O is
+// rarely rescaled (values stay <= 256 before normalisation).
+// Tiles are classified per Q tile from the document bounds of its rows:
+// SKIP (no valid pair: no load, no MMA), FULL (no mask), MASKED (per-row
+// interval mask).
+
+#include <cuda.h>
+
+#include "sp_device.cuh"
+
+namespace sp {
+namespace {
+
+constexpr int CLS_SKIP = 0, CLS_MASKED = 1, CLS_FULL = 2;
+
+template <int D>
+struct Cfg {
+  static constexpr int NSTAGE = 2;
+  static constexpr int KSUB = D / 64;             // 128-byte sub-tiles along d
+  static constexpr int SUB_BYTES = 128 * 128;     // [128 rows][64 bf16]
+  static constexpr int TILE_BYTES = KSUB * SUB_BYTES;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NSTAGE * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NSTAGE * TILE_BYTES;
+  static constexpr int N_BARS = 17;
+  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+  static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr int TM_S = 0;
+  static constexpr int TM_O = 256;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);
+};
+
+// Barrier slots.
+enum {
+  B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = 4, B_V_FULL = 6, B_V_EMPTY = 8,
+  B_S_FULL = 10, B_P_FULL = 12, B_O_FULL = 14, B_DRAIN = 16
+};
+
+struct QTile {
+  int qa, qb;   // valid rows [qa, qb) (empty when qa >= qb)
+  int ds, de;   // document start of row qa, document end of row qb-1
+  int one_doc;  // rows all in one document
+};
+
+__device__ __forceinline__ QTile make_qtile(const AttnArgs& a, const UnitInfo& ui, int i) {
+  QTile t;
+  t.qa = ui.q0 + 128 * i;
+  t.qb = min(t.qa + 128, ui.q_hi);
+  if (t.qb <= t.qa) {
+    t.qa = t.qb = 0;
+    t.ds = t.de = 0;
+    t.one_doc = 0;
+    return t;
+  }
+  const int d0 = doc_of(a.cu, a.ndocs, t.qa);
+  const int d1 = doc_of(a.cu, a.ndocs, t.qb - 1);
+  t.ds = __ldg(a.cu + d0);
+  t.de = __ldg(a.cu + d1 + 1);
+  t.one_doc = (d0 == d1);
+  return t;
+}
+
+__device__ __forceinline__ int classify(const QTile& t, int ka, int kb, int causal) {
+  if (t.qa >= t.qb) return CLS_SKIP;
+  if (causal && ka > t.qb - 1) return CLS_SKIP;
+  if (t.de <= ka || kb <= t.ds) return CLS_SKIP;
+  if (t.qb - t.qa == 128 && kb - ka == 128 && t.one_doc && ka >= t.ds && kb <= t.de &&
+      (!causal || kb - 1 <= t.qa))
+    return CLS_FULL;
+  return CLS_MASKED;
+}
+
+struct Cursor {
+  int item, item_end, kv_e, k0;
+};
+
+// Advances to the next 128-key tile of the unit that is not SKIP for both Q
+// tiles. Every role runs this same function, so all agree on the sequence.
+__device__ __forceinline__ bool next_tile(const AttnArgs& a, Cursor& c, const QTile (&qt)[2],
+                                          int& ka, int& kb, int (&cls)[2]) {
+  while (true) {
+    if (c.k0 >= c.kv_e) {
+      if (c.item >= c.item_end) return false;
+      int b, e;
+      item_range(a, c.item, b, e);
+      ++c.item;
+      c.k0 = b;
+      c.kv_e = e;
+      continue;
+    }
+    ka = c.k0;
+    kb = min(c.k0 + 128, c.kv_e);
+    c.k0 += 128;
+    cls[0] = classify(qt[0], ka, kb, a.causal);
+    cls[1] = classify(qt[1], ka, kb, a.causal);
+    if (cls[0] != CLS_SKIP || cls[1] != CLS_SKIP) return true;
+  }
+}
+
+template <int D, int OUT_FP32>
+__global__ void __launch_bounds__(384, 1)
+attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
+               const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_Q_FULL), 1);
+    mbar_init(bar(B_Q_EMPTY), 1);
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(bar(B_K_FULL + s), 1);
+      mbar_init(bar(B_K_EMPTY + s), 1);
+      mbar_init(bar(B_V_FULL + s), 1);
+      mbar_init(bar(B_V_EMPTY + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_S_FULL + i), 1);
+      mbar_init(bar(B_P_FULL + i), 4);
+      mbar_init(bar(B_O_FULL + i), 1);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_units = n_units_of(a);
+  const int G = a.Hq / a.Hkv;
+  const unsigned long long tmo = a.timeout_ns;
+
+  // Register split: the producer/MMA warpgroup needs few registers, the two
+  // softmax warpgroups hold a 128-column row of S each. 128*88 + 256*208 equals
+  // the 384*168 the block is launched with.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
+  }
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      uint32_t kv_cnt = 0, unit_cnt = 0;
+      int armed_k[C::NSTAGE] = {}, armed_v[C::NSTAGE] = {};
+      uint32_t par_k[C::NSTAGE] = {}, par_v[C::NSTAGE] = {};
+      int armed_q = 0;
+      uint32_t par_q = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+        const UnitInfo ui = unit_info(a, u);
+        const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
+        const int hk = ui.h / G;
+        if (!mbar_wait_bounded(bar(B_Q_EMPTY), (unit_cnt & 1) ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * C::TILE_BYTES);
+        armed_q = 1;
+        par_q = unit_cnt & 1;
+        for (int i = 0; i < 2; ++i)
+          for (int s = 0; s < C::KSUB; ++s)
+            tma_load_3d(sQ + i * C::TILE_BYTES + s * C::SUB_BYTES, &tmq, bar(B_Q_FULL), 64 * s,
+                        ui.h, ui.q0 + 128 * i);
+        Cursor cur{ui.item_lo, ui.item_hi, 0, 0};
+        int ka, kb, cls[2];
+        while (next_tile(a, cur, qt, ka, kb, cls)) {
+          const int st = kv_cnt % C::NSTAGE;
+          const uint32_t ph = (kv_cnt / C::NSTAGE) & 1;
+          if (!mbar_wait_bounded(bar(B_K_EMPTY + st), ph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(B_K_FULL + st), C::TILE_BYTES);
+          armed_k[st] = 1;
+          par_k[st] = ph;
+          for (int s = 0; s < C::KSUB; ++s)
+            tma_load_3d(sK + st * C::TILE_BYTES + s * C::SUB_BYTES, &tmk, bar(B_K_FULL + st), 64 * s,
+                        hk, ka);
+          if (!mbar_wait_bounded(bar(B_V_EMPTY + st), ph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(B_V_FULL + st), C::TILE_BYTES);
+          armed_v[st] = 1;
+          par_v[st] = ph;
+          for (int s = 0; s < C::KSUB; ++s)
+            tma_load_3d(sV + st * C::TILE_BYTES + s * C::SUB_BYTES, &tmv, bar(B_V_FULL + st), 64 * s,
+                        hk, ka);
+          ++kv_cnt;
+        }
+      }
+      if (!ok) {
+        // Aborting: let every copy already issued land before the block exits.
+        volatile int no_abort = 0;
+        const unsigned long long drain = 50000000ull;
+        if (armed_q) mbar_wait_bounded(bar(B_Q_FULL), par_q, drain, a.err, &no_abort);
+        for (int s = 0; s < C::NSTAGE; ++s) {
+          if (armed_k[s]) mbar_wait_bounded(bar(B_K_FULL + s), par_k[s], drain, a.err, &no_abort);
+          if (armed_v[s]) mbar_wait_bounded(bar(B_V_FULL + s), par_v[s], drain, a.err, &no_abort);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kv_cnt = 0, unit_cnt = 0, pcnt0 = 0, pcnt1 = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+        const UnitInfo ui = unit_info(a, u);
+        const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
+        if (!mbar_wait_bounded(bar(B_Q_FULL), unit_cnt & 1, tmo, a.err, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        int has_pv0 = 0, has_pv1 = 0;
+        int have_prev = 0, prev_st = 0, prev_cls1 = 0;
+        Cursor cur{ui.item_lo, ui.item_hi, 0, 0};
+        int ka, kb, cls[2];
+
+        auto issue_qk = [&](int i, int st) {
+          const uint32_t d_t = tmem + C::TM_S + 128 * i;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+            const uint64_t ad = smem_desc_sw128(sQ + i * C::TILE_BYTES + off, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(sK + st * C::TILE_BYTES + off, 16, 1024);
+            tc_mma_ss(d_t, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+        };
+        auto issue_pv = [&](int i, int st, int acc) {
+          const uint32_t d_t = tmem + C::TM_O + D * i;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a_t = tmem + C::TM_S + 128 * i + 64 + 8 * kk;
+            const uint64_t bd = smem_desc_sw128(sV + st * C::TILE_BYTES + kk * 2048, C::SUB_BYTES, 1024);
+            tc_mma_ts(d_t, a_t, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+          }
+        };
+
+        while (next_tile(a, cur, qt, ka, kb, cls)) {
+          const int st = kv_cnt % C::NSTAGE;
+          const uint32_t ph = (kv_cnt / C::NSTAGE) & 1;
+          if (!mbar_wait_bounded(bar(B_K_FULL + st), ph, tmo, a.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (cls[0] != CLS_SKIP) {
+            issue_qk(0, st);
+            tc_commit(bar(B_S_FULL + 0));
+          }
+          if (have_prev) {
+            if (prev_cls1 != CLS_SKIP) {
+              if (!mbar_wait_bounded(bar(B_P_FULL + 1), pcnt1 & 1, tmo, a.err, abort_flag)) { ok = false; break; }
+              ++pcnt1;
+              tc_fence_after();
+              issue_pv(1, prev_st, has_pv1);
+              has_pv1 = 1;
+            }
+            tc_commit(bar(B_V_EMPTY + prev_st));
+          }
+          if (cls[1] != CLS_SKIP) {
+            issue_qk(1, st);
+            tc_commit(bar(B_S_FULL + 1));
+          }
+          tc_commit(bar(B_K_EMPTY + st));
+          if (!mbar_wait_bounded(bar(B_V_FULL + st), ph, tmo, a.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (cls[0] != CLS_SKIP) {
+            if (!mbar_wait_bounded(bar(B_P_FULL + 0), pcnt0 & 1, tmo, a.err, abort_flag)) { ok = false; break; }
+            ++pcnt0;
+            tc_fence_after();
+            issue_pv(0, st, has_pv0);
+            has_pv0 = 1;
+          }
+          have_prev = 1;
+          prev_st = st;
+          prev_cls1 = cls[1];
+          ++kv_cnt;
+        }
+        if (!ok) break;
+        if (have_prev) {
+          if (prev_cls1 != CLS_SKIP) {
+            if (!mbar_wait_bounded(bar(B_P_FULL + 1), pcnt1 & 1, tmo, a.err, abort_flag)) { ok = false; break; }
+            ++pcnt1;
+            tc_fence_after();
+            issue_pv(1, prev_st, has_pv1);
+          }
+          tc_commit(bar(B_V_EMPTY + prev_st));
+        }
+        tc_commit(bar(B_Q_EMPTY));
+        tc_commit(bar(B_O_FULL + 0));
+        tc_commit(bar(B_O_FULL + 1));
+      }
+      // Every MMA issued has completed before tensor memory is released.
+      volatile int no_abort = 0;
+      tc_commit(bar(B_DRAIN));
+      mbar_wait_bounded(bar(B_DRAIN), 0, 50000000ull, a.err, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;");
+    const int wg = (warp - 4) >> 2;       // which Q tile
+    const int wq = warp & 3;              // tensor-memory lane quarter
+    const int r = wq * 32 + lane;         // row within the Q tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::TM_S + 128 * wg;
+    const uint32_t tO = tmem + lane_off + C::TM_O + D * wg;
+    const float sl2 = a.scale_log2;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    uint32_t s_cnt = 0, unit_cnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+      const UnitInfo ui = unit_info(a, u);
+      const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
+      const QTile my = wg ? qt[1] : qt[0];
+      const int t = ui.q0 + 128 * wg + r;
+      const bool valid = (t >= my.qa) && (t < my.qb);
+      int rds = 0, rde = 0;
+      if (valid) {
+        const int dd = doc_of(a.cu, a.ndocs, t);
+        rds = __ldg(a.cu + dd);
+        rde = __ldg(a.cu + dd + 1);
+      }
+      const int rcausal_end = a.causal ? t + 1 : 0x7fffffff;
+      float m = NEG_INF, l = 0.f;
+      int has_pv = 0;
+      Cursor cur{ui.item_lo, ui.item_hi, 0, 0};
+      int ka, kb, cls[2];
+      while (next_tile(a, cur, qt, ka, kb, cls)) {
+        const int c = wg ? cls[1] : cls[0];
+        if (c == CLS_SKIP) continue;
+        if (!mbar_wait_bounded(bar(B_S_FULL + wg), s_cnt & 1, tmo, a.err, abort_flag)) { ok = false; break; }
+        ++s_cnt;
+        tc_fence_after();
+        float s[128];
+        {
+          uint32_t rr[32];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            tmem_ld32_sync(tS + 32 * ch, rr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s[32 * ch + j] = __uint_as_float(rr[j]);
+          }
+        }
+        if (c == CLS_MASKED) {
+          int lo = 0, hi = 0;
+          if (valid) {
+            lo = max(ka, rds) - ka;
+            hi = min(min(kb, rde), rcausal_end) - ka;
+          }
+#pragma unroll
+          for (int j = 0; j < 128; ++j) s[j] = (j >= lo && j < hi) ? s[j] : NEG_INF;
+        }
+        float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int j = 4; j < 128; j += 4) {
+          mx[0] = fmaxf(mx[0], s[j]);
+          mx[1] = fmaxf(mx[1], s[j + 1]);
+          mx[2] = fmaxf(mx[2], s[j + 2]);
+          mx[3] = fmaxf(mx[3], s[j + 3]);
+        }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const float m_new = fmaxf(m, mt);
+        const bool need = m_new > m + 8.0f;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m - m_new);
+          l *= alpha;
+          m = m_new;
+        }
+        const float mu = (m == NEG_INF) ? 0.f : m;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk0[32], pk1[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float p0 = ex2_approx(fmaf(s[2 * j], sl2, -mu));
+          const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, -mu));
+          const float p2 = ex2_approx(fmaf(s[64 + 2 * j], sl2, -mu));
+          const float p3 = ex2_approx(fmaf(s[64 + 2 * j + 1], sl2, -mu));
+          ls[j & 1] += p0 + p1;
+          ls[2 + (j & 1)] += p2 + p3;
+          pk0[j] = pack_bf16x2(p0, p1);
+          pk1[j] = pack_bf16x2(p2, p3);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tmem_st32(tS + 64, pk0);
+        tmem_st32(tS + 96, pk1);
+        if (has_pv && __any_sync(0xffffffffu, need)) {
+          uint32_t rr[32];
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            tmem_ld32_sync(tO + 32 * ch, rr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+            tmem_st32(tO + 32 * ch, rr);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_P_FULL + wg));
+        has_pv = 1;
+      }
+      if (!ok) break;
+      // ---------------- epilogue: O = acc / l, LSE = ln 2 * (m + log2 l)
+      if (!mbar_wait_bounded(bar(B_O_FULL + wg), unit_cnt & 1, tmo, a.err, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const bool live = l > 0.f;
+      const float inv = live ? 1.f / l : 0.f;
+      const float lse_v = live ? (m + lg2_approx(l)) * 0.69314718055994531f : NEG_INF;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t rr[32];
+        if (has_pv) {
+          tmem_ld32_sync(tO + 32 * ch, rr);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rr[j] = 0u;
+        }
+        if (valid) {
+          if (OUT_FP32) {
+            float* dst = static_cast<float*>(a.o) +
+                         (static_cast<size_t>(t - a.row_base) * a.Hq + ui.h) * D + 32 * ch;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float4 v4 = make_float4(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv,
+                                      __uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
+              *reinterpret_cast<float4*>(dst + j) = v4;
+            }
+          } else {
+            uint16_t* dst = static_cast<uint16_t*>(a.o) +
+                            (static_cast<size_t>(t) * a.Hq + ui.h) * D + 32 * ch;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(rr[j + 4]) * inv, __uint_as_float(rr[j + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(rr[j + 6]) * inv, __uint_as_float(rr[j + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + j) = w;
+            }
+          }
+        }
+      }
+      if (valid) {
+        if (OUT_FP32)
+          a.lse[static_cast<size_t>(ui.h) * a.n_rows + (t - a.row_base)] = lse_v;
+        else
+          a.lse[static_cast<size_t>(ui.h) * a.T + t] = lse_v;
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, int OUT_FP32>
+cudaError_t launch_one(const AttnArgs& a, const void* tq, const void* tk, const void* tv, int grid,
+                       cudaStream_t st) {
+  using C = Cfg<D>;
+  auto kern = attn_tc_kernel<D, OUT_FP32>;
+  static int configured_mask = 0;  // per-device bit (devices < 32)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(configured_mask & (1 << (dev & 31)))) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    configured_mask |= 1 << (dev & 31);
+  }
+  CUtensorMap mq, mk, mv;
+  memcpy(&mq, tq, sizeof mq);
+  memcpy(&mk, tk, sizeof mk);
+  memcpy(&mv, tv, sizeof mv);
+  kern<<<grid, 384, C::SMEM_ALLOC, st>>>(a, mq, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const AttnArgs& a, const void* tq, const void* tk, const void* tv,
+                           int grid, cudaStream_t st) {
+  if (a.d == 128) return a.out_mode ? launch_one<128, 1>(a, tq, tk, tv, grid, st)
+                                    : launch_one<128, 0>(a, tq, tk, tv, grid, st);
+  return a.out_mode ? launch_one<64, 1>(a, tq, tk, tv, grid, st)
+                    : launch_one<64, 0>(a, tq, tk, tv, grid, st);
+}
+
+}  // namespace sp

@@ -1,0 +1,212 @@
+// Auxiliary kernels: the schedule set-up pass, the log-sum-exp merge of
+// partials, and the bounded-wait self-test.
+
+#include "sp_device.cuh"
+#include "sp_workspace.h"
+
+namespace sp {
+namespace {
+
+// Block-wide exclusive scan of one int64 per thread (1024 threads).
+__device__ long long block_exclusive_scan(long long x, long long* tmp, long long* total) {
+  const int tid = threadIdx.x;
+  tmp[tid] = x;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const long long y = (tid >= off) ? tmp[tid - off] : 0;
+    __syncthreads();
+    tmp[tid] += y;
+    __syncthreads();
+  }
+  const long long incl = tmp[tid];
+  *total = tmp[1023];
+  __syncthreads();
+  return incl - x;
+}
+
+// Groups the items by (rank, Q range) runs, estimates each group's cost
+// (row groups x 128-key tiles), orders groups largest first, and assigns
+// work-unit ranges. One block of 1024 threads. Also validates the items.
+__global__ void __launch_bounds__(1024)
+prep_kernel(const sp_item* __restrict__ items, int n, int T, int Hq, int rpu, int32_t* ws,
+            unsigned* err) {
+  __shared__ long long scan_tmp[1024];
+  __shared__ int bad;
+  const WsLayout L = ws_layout(n);
+  int32_t* header = ws;
+  SegEntry* segs = reinterpret_cast<SegEntry*>(reinterpret_cast<char*>(ws) + L.off_segs);
+  SegEntry* tmp = reinterpret_cast<SegEntry*>(reinterpret_cast<char*>(ws) + L.off_tmp);
+  int32_t* starts = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + L.off_starts);
+  long long* cost = reinterpret_cast<long long*>(reinterpret_cast<char*>(ws) + L.off_cost);
+  const int tid = threadIdx.x;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+
+  const int chunk = (n + 1023) / 1024;
+  const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
+  long long cnt = 0;
+  for (int i = i0; i < i1; ++i) {
+    const sp_item it = items[i];
+    if (!(0 <= it.q_begin && it.q_begin < it.q_end && it.q_end <= T && 0 <= it.kv_begin &&
+          it.kv_begin <= it.kv_end && it.kv_end <= T))
+      bad = 1;
+    bool start = (i == 0);
+    if (!start) {
+      const sp_item pv = items[i - 1];
+      start = pv.rank != it.rank || pv.q_begin != it.q_begin || pv.q_end != it.q_end;
+    }
+    cnt += start;
+  }
+  long long nseg_ll;
+  long long off = block_exclusive_scan(cnt, scan_tmp, &nseg_ll);
+  const int nseg = static_cast<int>(nseg_ll);
+  for (int i = i0; i < i1; ++i) {
+    bool start = (i == 0);
+    if (!start) {
+      const sp_item pv = items[i - 1], it = items[i];
+      start = pv.rank != it.rank || pv.q_begin != it.q_begin || pv.q_end != it.q_end;
+    }
+    if (start) starts[off++] = i;
+  }
+  if (tid == 0) starts[nseg] = n;
+  __syncthreads();
+
+  for (int s = tid; s < nseg; s += 1024) {
+    const int lo = starts[s], hi = starts[s + 1];
+    const sp_item first = items[lo];
+    long long tiles = 0;
+    for (int i = lo; i < hi; ++i) tiles += (items[i].kv_end - items[i].kv_begin + 127) / 128;
+    const int qg = (first.q_end - first.q_begin + rpu - 1) / rpu;
+    SegEntry e;
+    e.q_lo = first.q_begin;
+    e.q_hi = first.q_end;
+    e.item_lo = lo;
+    e.item_hi = hi;
+    e.unit_begin = 0;
+    e.n_qgroups = qg;
+    e.pad0 = e.pad1 = 0;
+    tmp[s] = e;
+    cost[s] = tiles * qg;
+  }
+  __syncthreads();
+
+  // Largest estimated cost first (ties keep schedule order).
+  const bool sorted = nseg <= 8192;
+  for (int s = tid; s < nseg; s += 1024) {
+    int rank = s;
+    if (sorted) {
+      rank = 0;
+      const long long cs = cost[s];
+      for (int t2 = 0; t2 < nseg; ++t2) {
+        const long long ct = cost[t2];
+        rank += (ct > cs) || (ct == cs && t2 < s);
+      }
+    }
+    segs[rank] = tmp[s];
+  }
+  __syncthreads();
+
+  // Q ranges of different groups must not overlap (each output row is
+  // written by exactly one group).
+  if (nseg <= 8192) {
+    for (int s = tid; s < nseg; s += 1024) {
+      const int a0 = segs[s].q_lo, a1 = segs[s].q_hi;
+      for (int t2 = s + 1; t2 < nseg; ++t2)
+        if (max(a0, segs[t2].q_lo) < min(a1, segs[t2].q_hi)) bad = 1;
+    }
+  }
+
+  // Work-unit prefix over the sorted groups.
+  const int schunk = (nseg + 1023) / 1024;
+  const int s0 = min(nseg, tid * schunk), s1 = min(nseg, s0 + schunk);
+  long long units = 0;
+  for (int s = s0; s < s1; ++s) units += static_cast<long long>(segs[s].n_qgroups) * Hq;
+  long long total;
+  long long ub = block_exclusive_scan(units, scan_tmp, &total);
+  for (int s = s0; s < s1; ++s) {
+    segs[s].unit_begin = static_cast<int32_t>(ub);
+    ub += static_cast<long long>(segs[s].n_qgroups) * Hq;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const bool fail = bad || total > 0x7fffffffll;
+    header[WS_N_SEGS] = fail ? 0 : nseg;
+    header[WS_N_UNITS] = fail ? 0 : static_cast<int32_t>(total);
+    header[WS_STATUS] = fail ? 1 : 0;
+    if (fail) atomicOr(err, ERR_INTERNAL_BIT);
+  }
+}
+
+// One warp per (row, head): fold partial 2 into accumulator 1 in place.
+__global__ void __launch_bounds__(256)
+lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
+                 const float* __restrict__ o_part, const float* __restrict__ lse_part, int rows,
+                 int Hq, int d) {
+  const int lane = threadIdx.x & 31;
+  const long long n = static_cast<long long>(rows) * Hq;
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       w < n; w += wstride) {
+    const int row = static_cast<int>(w / Hq), h = static_cast<int>(w % Hq);
+    const size_t li = static_cast<size_t>(h) * rows + row;
+    const float l1 = lse_acc[li], l2 = __ldg(lse_part + li);
+    const float M = fmaxf(l1, l2);
+    float w1, w2, L;
+    if (M == NEG_INF) {
+      w1 = w2 = 0.f;
+      L = NEG_INF;
+    } else {
+      const float e1 = expf(l1 - M), e2 = expf(l2 - M);
+      const float s = e1 + e2;
+      L = M + logf(s);
+      const float inv = 1.f / s;
+      w1 = e1 * inv;
+      w2 = e2 * inv;
+    }
+    float4* oa = reinterpret_cast<float4*>(o_acc + static_cast<size_t>(w) * d);
+    const float4* op = reinterpret_cast<const float4*>(o_part + static_cast<size_t>(w) * d);
+    for (int c = lane; c < (d >> 2); c += 32) {
+      const float4 x = oa[c], y = __ldg(op + c);
+      oa[c] = make_float4(w1 * x.x + w2 * y.x, w1 * x.y + w2 * y.y, w1 * x.z + w2 * y.z,
+                          w1 * x.w + w2 * y.w);
+    }
+    __syncwarp();
+    if (lane == 0) lse_acc[li] = L;
+  }
+}
+
+__global__ void wait_selftest_kernel(unsigned long long timeout_ns, unsigned* err) {
+  __shared__ __align__(8) unsigned long long barmem;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    const uint32_t bar = smem_u32(&barmem);
+    abort_flag = 0;
+    mbar_init(bar, 1);
+    mbar_fence_init();
+    // Nothing ever arrives on bar: the wait must give up on its own.
+    mbar_wait_bounded(bar, 0, timeout_ns, err, &abort_flag);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const sp_item* items, int64_t n_items, int32_t T, int32_t Hq,
+                        int32_t rows_per_unit, void* workspace, unsigned* err, cudaStream_t st) {
+  prep_kernel<<<1, 1024, 0, st>>>(items, static_cast<int>(n_items), T, Hq, rows_per_unit,
+                                  static_cast<int32_t*>(workspace), err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+                             int32_t rows, int32_t Hq, int32_t d, int grid, cudaStream_t st) {
+  lse_merge_kernel<<<grid, 256, 0, st>>>(o_acc, lse_acc, o_part, lse_part, rows, Hq, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(timeout_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace sp

@@ -1,0 +1,73 @@
+// Internal declarations shared by the translation units of libsp_attn.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/sp_attn.h"
+
+namespace sp {
+
+// Error bits recorded in the per-device error word.
+enum : unsigned { ERR_TIMEOUT_BIT = 1u, ERR_INTERNAL_BIT = 2u };
+
+// One group of items that share a rank and a Q range. After the set-up kernel
+// the table is sorted by estimated cost, largest first.
+struct SegEntry {
+  int32_t q_lo, q_hi;        // Q rows of the group
+  int32_t item_lo, item_hi;  // items [item_lo, item_hi) in schedule order
+  int32_t unit_begin;        // first work unit of the group
+  int32_t n_qgroups;         // row groups of rows_per_unit rows
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(SegEntry) == 32, "SegEntry is 32 bytes");
+
+// Workspace header (int32 words).
+enum : int { WS_N_SEGS = 0, WS_N_UNITS = 1, WS_STATUS = 2, WS_HEADER_WORDS = 16 };
+
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const int32_t* cu;
+  int32_t ndocs;
+  int32_t T, Hq, Hkv, d;
+  int32_t causal;
+  float scale;       // multiplies q.k
+  float scale_log2;  // scale * log2(e)
+  // Work description: either a device table produced by the set-up kernel
+  // (header != nullptr) or one inline group holding one inline item.
+  const sp_item* items;
+  const SegEntry* segs;
+  const int32_t* header;
+  sp_item inline_item;
+  SegEntry inline_seg;
+  int32_t inline_n_units;
+  int32_t rows_per_unit;
+  // Output: mode 0 writes O [T][Hq][d] (bf16 or fp32) and LSE [Hq][T];
+  // mode 1 writes fp32 O [t - row_base][Hq][d] and LSE [Hq][n_rows].
+  int32_t out_mode;
+  int32_t row_base, n_rows;
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+// Launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_prep(const sp_item* items, int64_t n_items, int32_t T, int32_t Hq,
+                        int32_t rows_per_unit, void* workspace, unsigned* err, cudaStream_t st);
+cudaError_t launch_attn_simt(const AttnArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_attn_tc(const AttnArgs& a, const void* tmap_q, const void* tmap_k,
+                           const void* tmap_v, int grid, cudaStream_t st);
+cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+                             int32_t rows, int32_t Hq, int32_t d, int grid, cudaStream_t st);
+cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t st);
+
+// Rows per work unit of each kernel.
+constexpr int TC_ROWS_PER_UNIT = 256;
+constexpr int SIMT_ROWS_PER_UNIT = 128;
+
+}  // namespace sp

@@ -1,0 +1,401 @@
+// Host-side chunk-visit schedules for virtual sequence-parallel ranks.
+//
+// RING follows the Ring AllGather order of Ring Attention, ZIGZAG its
+// Zigzag-Ring variant, and TASP the topology decomposition (P-1 arc-disjoint
+// directed Hamiltonian cycles of the complete digraph on P ranks) with the
+// primitive decomposition (each KV chunk cut into P-1 pieces, piece c relayed
+// on ring c) — "TASP: Topology-aware Sequence Parallelism", abstract. Items
+// without a valid (query, key) pair are pruned, the plainest reading of
+// sequence-aware scheduling of incomplete QKV on packed sequences ("HSAP",
+// abstract and method summary).
+//
+// The Hamiltonian decomposition is found by a seeded randomized search: whole
+// cycles are drawn by depth-first search with a fewest-exits-first order, and
+// the last two cycles are split exactly from the 2-regular remainder by
+// enumerating its perfect matchings. Everything is integer arithmetic, so the
+// result is identical on every host for a given (P, seed). Complete digraphs
+// on 4 and 6 vertices have no such decomposition (a result of graph theory,
+// not of the pages); every other P does.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "../../include/sp_attn.h"
+
+namespace {
+
+struct Rng {  // splitmix64
+  uint64_t s;
+  explicit Rng(uint64_t seed) : s(seed) {}
+  uint64_t next() {
+    uint64_t z = (s += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+  }
+  uint32_t below(uint32_t n) { return static_cast<uint32_t>(next() % n); }
+};
+
+inline int popc(uint64_t x) { return __builtin_popcountll(x); }
+inline uint64_t bit(int v) { return 1ull << v; }
+
+// Randomised DFS for a directed Hamiltonian cycle through vertex 0 in the
+// digraph given by out/in masks. Returns true and fills succ on success.
+struct HamSearch {
+  int P;
+  const uint64_t* out;
+  const uint64_t* in;
+  Rng* rng;
+  long long budget;
+  std::vector<int> path;
+
+  bool feasible(uint64_t unvisited, int cur) const {
+    // Every unvisited vertex still needs an entry from cur/unvisited and an
+    // exit to unvisited/vertex 0.
+    uint64_t from = unvisited | bit(cur);
+    uint64_t to = unvisited | bit(0);
+    for (uint64_t m = unvisited; m; m &= m - 1) {
+      int w = __builtin_ctzll(m);
+      if (!(in[w] & from) || !(out[w] & to)) return false;
+    }
+    return true;
+  }
+
+  bool dfs(int cur, uint64_t unvisited) {
+    if (--budget < 0) return false;
+    if (!unvisited) return (out[cur] & bit(0)) != 0;
+    uint64_t cand = out[cur] & unvisited;
+    if (!cand) return false;
+    int vs[64], keys[64], n = 0;
+    for (uint64_t m = cand; m; m &= m - 1) {
+      int v = __builtin_ctzll(m);
+      vs[n] = v;
+      // fewest onward exits first, random tie break
+      keys[n] = popc(out[v] & (unvisited & ~bit(v))) * 1024 + static_cast<int>(rng->below(1024));
+      ++n;
+    }
+    for (int a = 1; a < n; ++a)
+      for (int b = a; b > 0 && keys[b] < keys[b - 1]; --b) {
+        std::swap(keys[b], keys[b - 1]);
+        std::swap(vs[b], vs[b - 1]);
+      }
+    for (int x = 0; x < n; ++x) {
+      int v = vs[x];
+      uint64_t rest = unvisited & ~bit(v);
+      if (rest && !feasible(rest, v)) continue;
+      path.push_back(v);
+      if (dfs(v, rest)) return true;
+      path.pop_back();
+      if (budget < 0) return false;
+    }
+    return false;
+  }
+
+  bool run(std::vector<int>& succ) {
+    path.clear();
+    path.push_back(0);
+    uint64_t all = (P == 64) ? ~0ull : (bit(P) - 1);
+    if (!dfs(0, all & ~bit(0))) return false;
+    succ.assign(P, -1);
+    for (int i = 0; i < P; ++i) succ[path[i]] = path[(i + 1) % P];
+    return true;
+  }
+};
+
+bool single_cycle(const std::vector<int>& succ) {
+  const int P = static_cast<int>(succ.size());
+  int u = 0;
+  for (int i = 1; i < P; ++i) {
+    u = succ[u];
+    if (u == 0) return false;
+  }
+  return succ[u] == 0;
+}
+
+// Splits a 2-in/2-out regular digraph into two Hamiltonian cycles, if possible.
+bool split_two(int P, const uint64_t* out, std::vector<int>& a, std::vector<int>& b) {
+  // Components of the bipartite (tail, head) graph: alternate "first arc of a
+  // tail" / "other in-arc of its head" until the walk closes.
+  std::vector<std::vector<std::pair<int, int>>> comps;  // arcs in walk order
+  std::vector<char> seen_tail(P, 0);
+  std::vector<int> in_a(P, -1), in_b(P, -1);  // the two tails entering each head
+  for (int u = 0; u < P; ++u)
+    for (uint64_t m = out[u]; m; m &= m - 1) {
+      int v = __builtin_ctzll(m);
+      if (in_a[v] < 0) in_a[v] = u; else in_b[v] = u;
+    }
+  for (int u0 = 0; u0 < P; ++u0) {
+    if (seen_tail[u0]) continue;
+    std::vector<std::pair<int, int>> arcs;
+    int u = u0;
+    int v = __builtin_ctzll(out[u]);
+    while (true) {
+      seen_tail[u] = 1;
+      arcs.push_back({u, v});               // even position: option 0
+      int u2 = (in_a[v] == u) ? in_b[v] : in_a[v];
+      uint64_t o2 = out[u2] & ~bit(v);
+      int v2 = __builtin_ctzll(o2);
+      arcs.push_back({u2, v});              // odd position: option 1
+      seen_tail[u2] = 1;
+      if (u2 == u0) break;
+      u = u2;
+      v = v2;
+    }
+    comps.push_back(arcs);
+  }
+  const int nc = static_cast<int>(comps.size());
+  if (nc > 22) return false;
+  a.assign(P, -1);
+  b.assign(P, -1);
+  for (uint32_t mask = 0; mask < (1u << nc); ++mask) {
+    for (int c = 0; c < nc; ++c) {
+      const int pick = (mask >> c) & 1;
+      const auto& arcs = comps[c];
+      for (size_t i = 0; i < arcs.size(); ++i) {
+        if (static_cast<int>(i & 1) == pick) a[arcs[i].first] = arcs[i].second;
+        else b[arcs[i].first] = arcs[i].second;
+      }
+    }
+    if (single_cycle(a) && single_cycle(b)) return true;
+  }
+  return false;
+}
+
+bool decompose(int P, uint64_t seed, std::vector<int>& table) {
+  table.clear();
+  if (P <= 1) return true;
+  if (P == 4 || P == 6 || P > 64) return false;
+  const uint64_t all = (P == 64) ? ~0ull : (bit(P) - 1);
+  Rng rng(seed ^ (0xA24BAED4963EE407ull * static_cast<uint64_t>(P)));
+  for (int attempt = 0; attempt < 2000; ++attempt) {
+    std::vector<uint64_t> out(P), in(P);
+    for (int u = 0; u < P; ++u) out[u] = in[u] = all & ~bit(u);
+    std::vector<std::vector<int>> cycles;
+    bool ok = true;
+    while (ok) {
+      const int k = P - 1 - static_cast<int>(cycles.size());  // current degree
+      if (k == 0) break;
+      if (k == 1) {  // only possible for P == 2
+        std::vector<int> s(P);
+        for (int u = 0; u < P; ++u) s[u] = __builtin_ctzll(out[u]);
+        if (!single_cycle(s)) { ok = false; break; }
+        cycles.push_back(s);
+        break;
+      }
+      if (k == 2) {
+        std::vector<int> a, b;
+        if (!split_two(P, out.data(), a, b)) { ok = false; break; }
+        cycles.push_back(a);
+        cycles.push_back(b);
+        break;
+      }
+      // k >= 3: draw a Hamiltonian cycle; at k == 3 keep drawing until the
+      // 2-regular remainder splits.
+      const int tries = (k == 3) ? 400 : 1;
+      bool got = false;
+      for (int t = 0; t < tries && !got; ++t) {
+        HamSearch hs{P, out.data(), in.data(), &rng, 200000, {}};
+        std::vector<int> s;
+        if (!hs.run(s)) continue;
+        if (k == 3) {
+          std::vector<uint64_t> o2 = out;
+          for (int u = 0; u < P; ++u) o2[u] &= ~bit(s[u]);
+          std::vector<int> a, b;
+          if (!split_two(P, o2.data(), a, b)) continue;
+        }
+        for (int u = 0; u < P; ++u) {
+          out[u] &= ~bit(s[u]);
+          in[s[u]] &= ~bit(u);
+        }
+        cycles.push_back(s);
+        got = true;
+      }
+      if (!got) ok = false;
+    }
+    if (ok && static_cast<int>(cycles.size()) == P - 1) {
+      table.resize(static_cast<size_t>(P - 1) * P);
+      for (int c = 0; c < P - 1; ++c)
+        for (int u = 0; u < P; ++u) table[static_cast<size_t>(c) * P + u] = cycles[c][u];
+      return true;
+    }
+  }
+  return false;
+}
+
+std::mutex g_cache_mu;
+std::map<std::pair<int, uint64_t>, std::vector<int>> g_cache;
+
+bool cached_decomposition(int P, uint64_t seed, std::vector<int>& table) {
+  {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    auto it = g_cache.find({P, seed});
+    if (it != g_cache.end()) { table = it->second; return true; }
+  }
+  if (!decompose(P, seed, table)) return false;
+  std::lock_guard<std::mutex> lk(g_cache_mu);
+  g_cache[{P, seed}] = table;
+  return true;
+}
+
+void split_bounds(int n, int parts, int idx, int* b, int* e) {
+  const int base = n / parts, extra = n % parts;
+  *b = idx * base + std::min(idx, extra);
+  *e = *b + base + (idx < extra ? 1 : 0);
+}
+
+struct Docs {
+  const int32_t* cu;
+  int nd;
+  int doc_of(int t) const {
+    int lo = 0, hi = nd - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) / 2;
+      if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  }
+  // True if some query in [qa,qb) may attend some key in [ka,kb).
+  bool any_valid(int qa, int qb, int ka, int kb, bool causal) const {
+    if (qa >= qb || ka >= kb) return false;
+    if (causal && ka > qb - 1) return false;
+    for (int D = doc_of(qa); D < nd && cu[D] < qb; ++D) {
+      const int r1 = std::min(qb, cu[D + 1]);
+      const int c0 = std::max(ka, cu[D]), c1 = std::min(kb, cu[D + 1]);
+      if (c0 >= c1) continue;
+      if (!causal || c0 <= r1 - 1) return true;
+    }
+    return false;
+  }
+  int flags(int qa, int qb, int ka, int kb, bool causal) const {
+    int f = 0;
+    if (causal && kb - 1 > qa) f |= SP_ITEM_CAUSAL_EDGE;
+    const int lo = std::min(qa, ka), hi = std::max(qb, kb) - 1;
+    if (doc_of(lo) != doc_of(hi)) f |= SP_ITEM_DOC_EDGE;
+    return f;
+  }
+};
+
+bool valid_cu(const int32_t* cu, int nd, int T) {
+  if (!cu || nd < 1 || cu[0] != 0 || cu[nd] != T) return false;
+  for (int i = 0; i < nd; ++i)
+    if (cu[i + 1] <= cu[i]) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sp_status_string(sp_status s) {
+  switch (s) {
+    case SP_OK: return "SP_OK";
+    case SP_ERR_INVALID_ARG: return "SP_ERR_INVALID_ARG";
+    case SP_ERR_UNSUPPORTED: return "SP_ERR_UNSUPPORTED";
+    case SP_ERR_BUFFER_TOO_SMALL: return "SP_ERR_BUFFER_TOO_SMALL";
+    case SP_ERR_CUDA: return "SP_ERR_CUDA";
+    case SP_ERR_TIMEOUT: return "SP_ERR_TIMEOUT";
+    case SP_ERR_INTERNAL: return "SP_ERR_INTERNAL";
+  }
+  return "SP_ERR_UNKNOWN";
+}
+
+sp_status sp_tasp_cycles(int32_t P, uint64_t seed, int32_t* out_succ) {
+  if (P < 1) return SP_ERR_INVALID_ARG;
+  if (P == 4 || P == 6 || P > 64) return SP_ERR_UNSUPPORTED;
+  if (P == 1) return SP_OK;
+  if (!out_succ) return SP_ERR_INVALID_ARG;
+  std::vector<int> table;
+  if (!cached_decomposition(P, seed, table)) return SP_ERR_INTERNAL;
+  for (size_t i = 0; i < table.size(); ++i) out_succ[i] = table[i];
+  return SP_OK;
+}
+
+sp_status sp_schedule_build(sp_sched_kind kind, int32_t P, int32_t T, const int32_t* cu,
+                            int32_t ndocs, int32_t causal_i, uint64_t seed, sp_item* out,
+                            int64_t* inout_n) {
+  if (!inout_n || P < 1 || T < 0) return SP_ERR_INVALID_ARG;
+  if (kind != SP_SCHED_RING && kind != SP_SCHED_ZIGZAG && kind != SP_SCHED_TASP)
+    return SP_ERR_INVALID_ARG;
+  if (T == 0) {
+    if (ndocs != 0 || (cu && cu[0] != 0)) return SP_ERR_INVALID_ARG;
+    *inout_n = 0;
+    return SP_OK;
+  }
+  if (!valid_cu(cu, ndocs, T)) return SP_ERR_INVALID_ARG;
+  if (kind == SP_SCHED_ZIGZAG && (T % (2 * P)) != 0) return SP_ERR_UNSUPPORTED;
+  if (kind == SP_SCHED_TASP && (P == 4 || P == 6 || P > 64)) return SP_ERR_UNSUPPORTED;
+  const bool causal = causal_i != 0;
+  Docs docs{cu, ndocs};
+
+  std::vector<int> succ;
+  std::vector<int> pred;
+  if (kind == SP_SCHED_TASP && P > 1) {
+    if (!cached_decomposition(P, seed, succ)) return SP_ERR_INTERNAL;
+    pred.assign(succ.size(), 0);
+    for (int c = 0; c < P - 1; ++c)
+      for (int u = 0; u < P; ++u)
+        pred[static_cast<size_t>(c) * P + succ[static_cast<size_t>(c) * P + u]] = u;
+  }
+
+  std::vector<sp_item> items;
+  auto emit = [&](int r, int s, int c, int qa, int qb, int ka, int kb) {
+    if (!docs.any_valid(qa, qb, ka, kb, causal)) return;
+    sp_item it{r, s, c, qa, qb, ka, kb, docs.flags(qa, qb, ka, kb, causal)};
+    items.push_back(it);
+  };
+
+  for (int r = 0; r < P; ++r) {
+    if (kind == SP_SCHED_RING) {
+      int qa, qb;
+      split_bounds(T, P, r, &qa, &qb);
+      for (int s = 0; s < P; ++s) {
+        int ka, kb;
+        split_bounds(T, P, ((r - s) % P + P) % P, &ka, &kb);
+        emit(r, s, 0, qa, qb, ka, kb);
+      }
+    } else if (kind == SP_SCHED_ZIGZAG) {
+      const int c = T / (2 * P);
+      const int mine[2] = {r, 2 * P - 1 - r};
+      for (int a = 0; a < 2; ++a)
+        for (int s = 0; s < P; ++s) {
+          const int src = ((r - s) % P + P) % P;
+          const int held[2] = {src, 2 * P - 1 - src};
+          for (int b = 0; b < 2; ++b)
+            emit(r, s, 0, mine[a] * c, (mine[a] + 1) * c, held[b] * c, (held[b] + 1) * c);
+        }
+    } else {
+      int qa, qb;
+      split_bounds(T, P, r, &qa, &qb);
+      emit(r, 0, 0, qa, qb, qa, qb);
+      for (int t = 1; t < P; ++t)
+        for (int c = 0; c < P - 1; ++c) {
+          int src = r;
+          for (int h = 0; h < t; ++h) src = pred[static_cast<size_t>(c) * P + src];
+          int cb, ce, pb, pe;
+          split_bounds(T, P, src, &cb, &ce);
+          split_bounds(ce - cb, P - 1, c, &pb, &pe);
+          emit(r, t, c, qa, qb, cb + pb, cb + pe);
+        }
+    }
+  }
+
+  const int64_t n = static_cast<int64_t>(items.size());
+  if (!out) {
+    *inout_n = n;
+    return SP_OK;
+  }
+  if (*inout_n < n) {
+    *inout_n = n;
+    return SP_ERR_BUFFER_TOO_SMALL;
+  }
+  if (n) std::memcpy(out, items.data(), sizeof(sp_item) * static_cast<size_t>(n));
+  *inout_n = n;
+  return SP_OK;
+}
+
+}  // extern "C"

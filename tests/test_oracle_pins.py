@@ -279,3 +279,16 @@ def test_valid_pair_counts():
             brute = sum(1 for i in range(qa, qb) for j in range(ka, kb)
                         if doc[i] == doc[j] and (not causal or j <= i))
             assert oracle.valid_pairs(cu, causal, int(qa), int(qb), int(ka), int(kb)) == brute
+
+
+def test_rows_only_query_layout():
+    rng = np.random.default_rng(8)
+    T, Hq, Hkv, d = 50, 2, 1, 8
+    cu = np.array([0, 20, 50], dtype=np.int32)
+    q = rng.standard_normal((T, Hq, d))
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    rows = np.array([49, 3, 20, 19])
+    o1, l1 = oracle.attn(q, k, v, cu, True, rows=rows)
+    o2, l2 = oracle.attn(q[rows], k, v, cu, True, rows=rows, q_rows_only=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
