@@ -31,7 +31,9 @@ def max_errs(o_gpu_rows, lse_gpu_rows, o_ref, lse_ref):
     """o_gpu_rows [n, Hq, d], lse_gpu_rows [n, Hq] (float64 numpy)."""
     eo = float(np.max(np.abs(o_gpu_rows - o_ref))) if o_ref.size else 0.0
     both_inf = np.isneginf(lse_gpu_rows) & np.isneginf(lse_ref)
-    diff = np.where(both_inf, 0.0, np.abs(lse_gpu_rows - lse_ref))
+    a = np.where(both_inf, 0.0, lse_gpu_rows)
+    b = np.where(both_inf, 0.0, lse_ref)
+    diff = np.abs(a - b)
     el = float(np.max(diff)) if diff.size else 0.0
     return eo, el
 
