@@ -161,6 +161,34 @@ sp_status sp_packed_attention(const void* q, const void* k, const void* v, void*
                               const sp_item* items_dev, int64_t n_items, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* sp_packed_attention_static_ws — sp_packed_attention for callers that cannot
+ * allocate device memory. The pages have no counterpart to this call.
+ *
+ * Some callers have no way to obtain the scratch buffer sp_packed_attention
+ * asks for: a plugin that is handed only its input and output pointers by a
+ * host framework that owns all device memory, a binding with no CUDA
+ * allocator of its own, or a serving loop that must not call cudaMalloc or
+ * cudaFree (which synchronise the device) once it is running. This variant
+ * takes the same arguments without the workspace and uses instead a fixed
+ * scratch array of SP_STATIC_WS_BYTES compiled into the library; every GPU
+ * that loads the library reserves that array until the process exits.
+ *  - Limit: n_items <= SP_STATIC_WS_MAX_ITEMS; longer schedules are rejected
+ *    with SP_ERR_BUFFER_TOO_SMALL before anything is launched.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - All calls on a device share the one array. The set-up kernel rewrites
+ *    every word the attention kernel reads, so nothing is carried over from
+ *    the previous call, but two calls whose work overlaps on the GPU (for
+ *    example on two streams) race on the array: serialise them.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define SP_STATIC_WS_BYTES (4u << 20)
+#define SP_STATIC_WS_MAX_ITEMS 40000
+sp_status sp_packed_attention_static_ws(const void* q, const void* k, const void* v, void* o, float* lse,
+                                        int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,
+                                        const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal,
+                                        float scale, const sp_item* items_dev, int64_t n_items,
+                                        void* stream);
+
 /* Synchronises `stream`, reads and clears the current device's error word, and
  * returns SP_OK, SP_ERR_TIMEOUT, SP_ERR_INTERNAL, or SP_ERR_CUDA when the
  * stream itself reports a CUDA error. */

@@ -26,7 +26,8 @@ _STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_
            4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_INTERNAL"}
 
 EXPORTED = ["sp_schedule_build", "sp_tasp_cycles", "sp_partial_attn", "sp_lse_merge",
-            "sp_packed_attention_workspace_size", "sp_packed_attention", "sp_check_device_status",
+            "sp_packed_attention_workspace_size", "sp_packed_attention",
+            "sp_packed_attention_static_ws", "sp_check_device_status",
             "sp_selftest_bounded_wait", "sp_status_string"]
 
 
@@ -69,6 +70,9 @@ def load():
         lib.sp_packed_attention.restype = ctypes.c_int
         lib.sp_packed_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int,
                                             vp, i32, i32, f32, vp, i64, vp, ctypes.c_size_t, vp]
+        lib.sp_packed_attention_static_ws.restype = ctypes.c_int
+        lib.sp_packed_attention_static_ws.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                      ctypes.c_int, vp, i32, i32, f32, vp, i64, vp]
         lib.sp_check_device_status.restype = ctypes.c_int
         lib.sp_check_device_status.argtypes = [vp]
         lib.sp_selftest_bounded_wait.restype = ctypes.c_int
@@ -207,6 +211,28 @@ def sp_packed_attention(q, k, v, o, lse, cu_seqlens, causal: bool, items_dev, wo
                                       int(causal), scale, _ptr(items_dev), items_dev.shape[0],
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "sp_packed_attention")
+
+
+def sp_packed_attention_static_ws(q, k, v, o, lse, cu_seqlens, causal: bool, items_dev,
+                                  scale: float | None = None, stream=None):
+    """sp_packed_attention without a caller workspace, for callers that cannot
+    allocate device memory: the library's fixed scratch array is used instead
+    (schedules of at most SP_STATIC_WS_MAX_ITEMS items; calls that overlap on
+    the GPU race on that array)."""
+    T, Hq, Hkv, d = _check_qkv(q, k, v)
+    torch = _torch()
+    _need(o.dtype == q.dtype and tuple(o.shape) == (T, Hq, d) and o.is_contiguous(), "o: [T, Hq, d]")
+    _need(lse.dtype == torch.float32 and tuple(lse.shape) == (Hq, T) and lse.is_contiguous(),
+          "lse must be fp32 [Hq, T]")
+    _need(items_dev.dtype == torch.int32 and items_dev.is_cuda and items_dev.dim() == 2 and
+          items_dev.shape[1] == 8 and items_dev.is_contiguous(), "items_dev: int32 [n, 8] on device")
+    _need(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_cuda, "cu_seqlens must be int32 on device")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    _check(load().sp_packed_attention_static_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, Hq,
+                                                Hkv, d, _dtype_code(q), _ptr(cu_seqlens),
+                                                cu_seqlens.numel() - 1, int(causal), scale,
+                                                _ptr(items_dev), items_dev.shape[0],
+                                                _stream(stream)), "sp_packed_attention_static_ws")
 
 
 def sp_check_device_status(stream=None):

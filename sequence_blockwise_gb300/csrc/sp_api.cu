@@ -253,3 +253,44 @@ sp_status sp_selftest_bounded_wait(uint64_t timeout_ns_arg, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the workspace is a fixed array in this module.
+
+namespace {
+
+// Scratch shared by every sp_packed_attention_static_ws call on a device. Host
+// code must not use the symbol itself as a pointer (it names a host-side
+// stand-in); it uses the device address looked up once per device below.
+static __device__ __align__(256) unsigned char g_static_ws[SP_STATIC_WS_BYTES];
+
+std::mutex g_static_mu;
+void* g_static_ws_dev[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" sp_status sp_packed_attention_static_ws(const void* q, const void* k, const void* v, void* o,
+                                                   float* lse, int32_t T, int32_t Hq, int32_t Hkv,
+                                                   int32_t d, sp_dtype dtype,
+                                                   const int32_t* cu_seqlens_dev, int32_t ndocs,
+                                                   int32_t causal, float scale,
+                                                   const sp_item* items_dev, int64_t n_items,
+                                                   void* stream) {
+  if (n_items > SP_STATIC_WS_MAX_ITEMS ||
+      sp_packed_attention_workspace_size(n_items) > SP_STATIC_WS_BYTES)
+    return SP_ERR_BUFFER_TOO_SMALL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SP_ERR_CUDA;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ws_dev[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return SP_ERR_CUDA;
+      g_static_ws_dev[dev] = p;
+    }
+    ws = g_static_ws_dev[dev];
+  }
+  return sp_packed_attention(q, k, v, o, lse, T, Hq, Hkv, d, dtype, cu_seqlens_dev, ndocs, causal,
+                             scale, items_dev, n_items, ws, SP_STATIC_WS_BYTES, stream);
+}
