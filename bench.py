@@ -326,6 +326,35 @@ def run_ours(args, world, rank, local):
     return result, w, cu
 
 
+def kernel_only(args, local):
+    """W warm-up and K timed steps of the device-resident path, nothing else:
+    the command the ncu summaries under profiles/ were taken with."""
+    import torch
+    import sequence_blockwise_gb300 as sb
+    from sequence_blockwise_gb300 import workloads as wl
+    w = wl.WORKLOADS[WORKLOAD_INDEX]
+    cu = wl.cu_seqlens(w)
+    dev = torch.device("cuda", local)
+    q, k, v = wl.make_qkv(w, dev)
+    att = sb.PackedAttention(cu, w.causal, w.kind, w.P, w.Hq, seed=w.seed, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        att(q, k, v, o, lse)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        att(q, k, v, o, lse)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    sb.sp_check_device_status()
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    flop = 4.0 * w.d * w.Hq * valid_pairs(cu, w.causal)
+    print(json.dumps({"kernel_only": True, "workload": w.name, "ms_per_step": ms,
+                      "tflops": flop / (ms * 1e-3) / 1e12}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -335,6 +364,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="only W warm-up + K device-resident steps (driver for ncu captures)")
     args = ap.parse_args()
 
     world, rank, local = dist_setup()
@@ -371,6 +402,10 @@ def main():
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
+        return
+
+    if args.kernel_only:
+        kernel_only(args, local)
         return
 
     result, w, cu = run_ours(args, world, rank, local)

@@ -173,10 +173,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const unsigned long long tmo = a.timeout_ns;
 
   // Register split: the producer/MMA warpgroup needs few registers, the two
-  // softmax warpgroups hold a 128-column row of S each. 128*88 + 256*208 equals
+  // softmax warpgroups hold a 128-column row of S each. 128*104 + 256*200 equals
   // the 384*168 the block is launched with.
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
   }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -239,6 +239,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(sQ + C::TILE_BYTES, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sV, C::SUB_BYTES, 1024);
       uint32_t kv_cnt = 0, unit_cnt = 0, pcnt0 = 0, pcnt1 = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
@@ -251,24 +255,26 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         Cursor cur{ui.item_lo, ui.item_hi, 0, 0};
         int ka, kb, cls[2];
 
+        // Descriptor bases are computed once; per MMA only the 14-bit start
+        // address field (bits [0,14), in 16-byte units) advances, by one add.
         auto issue_qk = [&](int i, int st) {
           const uint32_t d_t = tmem + C::TM_S + 128 * i;
+          const uint64_t a0 = i ? dq1 : dq0;
+          const uint64_t b0 = dk0 + static_cast<uint64_t>(st * (C::TILE_BYTES >> 4));
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-            const uint64_t ad = smem_desc_sw128(sQ + i * C::TILE_BYTES + off, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(sK + st * C::TILE_BYTES + off, 16, 1024);
-            tc_mma_ss(d_t, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::SUB_BYTES + (kk & 3) * 32) >> 4);
+            tc_mma_ss(d_t, a0 + off, b0 + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
           }
         };
         auto issue_pv = [&](int i, int st, int acc) {
           const uint32_t d_t = tmem + C::TM_O + D * i;
+          const uint32_t a_t = tmem + C::TM_S + 128 * i + 64;
+          const uint64_t b0 = dv0 + static_cast<uint64_t>(st * (C::TILE_BYTES >> 4));
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t a_t = tmem + C::TM_S + 128 * i + 64 + 8 * kk;
-            const uint64_t bd = smem_desc_sw128(sV + st * C::TILE_BYTES + kk * 2048, C::SUB_BYTES, 1024);
-            tc_mma_ts(d_t, a_t, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_ts(d_t, a_t + 8 * kk, b0 + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV,
+                      (acc || kk > 0) ? 1u : 0u);
         };
 
         while (next_tile(a, cur, qt, ka, kb, cls)) {
@@ -331,7 +337,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
     const int wg = (warp - 4) >> 2;       // which Q tile
     const int wq = warp & 3;              // tensor-memory lane quarter
     const int r = wq * 32 + lane;         // row within the Q tile
@@ -365,16 +371,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         if (!mbar_wait_bounded(bar(B_S_FULL + wg), s_cnt & 1, tmo, a.err, abort_flag)) { ok = false; break; }
         ++s_cnt;
         tc_fence_after();
-        float s[128];
-        {
-          uint32_t rr[32];
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            tmem_ld32_sync(tS + 32 * ch, rr);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) s[32 * ch + j] = __uint_as_float(rr[j]);
-          }
-        }
+        uint32_t sr[128];
+        tmem_ld128_sync(tS, sr);
         if (c == CLS_MASKED) {
           int lo = 0, hi = 0;
           if (valid) {
@@ -382,17 +380,20 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
             hi = min(min(kb, rde), rcausal_end) - ka;
           }
 #pragma unroll
-          for (int j = 0; j < 128; ++j) s[j] = (j >= lo && j < hi) ? s[j] : NEG_INF;
+          for (int j = 0; j < 128; ++j)
+            sr[j] = (j >= lo && j < hi) ? sr[j] : __float_as_uint(NEG_INF);
         }
-        float mx[4] = {s[0], s[1], s[2], s[3]};
+        // Row maximum: four independent chains of 3-input max.
+        float mx[4];
 #pragma unroll
-        for (int j = 4; j < 128; j += 4) {
-          mx[0] = fmaxf(mx[0], s[j]);
-          mx[1] = fmaxf(mx[1], s[j + 1]);
-          mx[2] = fmaxf(mx[2], s[j + 2]);
-          mx[3] = fmaxf(mx[3], s[j + 3]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float acc = __uint_as_float(sr[32 * q4]);
+#pragma unroll
+          for (int j = 1; j < 31; j += 2)
+            acc = fmax3f(acc, __uint_as_float(sr[32 * q4 + j]), __uint_as_float(sr[32 * q4 + j + 1]));
+          mx[q4] = fmaxf(acc, __uint_as_float(sr[32 * q4 + 31]));
         }
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const float mt = fmax3f(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
         const float m_new = fmaxf(m, mt);
         const bool need = m_new > m + 8.0f;
         float alpha = 1.f;
@@ -402,22 +403,31 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           m = m_new;
         }
         const float mu = (m == NEG_INF) ? 0.f : m;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk0[32], pk1[32];
+        // p = 2^(s * scale * log2 e - m): packed FMA, then MUFU ex2, packed
+        // row-sum, bf16 pairs written back over columns [64, 128) of S.
+        const uint64_t sc2 = f2_pack(sl2, sl2);
+        const uint64_t nm2 = f2_pack(-mu, -mu);
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[64];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = ex2_approx(fmaf(s[2 * j], sl2, -mu));
-          const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, -mu));
-          const float p2 = ex2_approx(fmaf(s[64 + 2 * j], sl2, -mu));
-          const float p3 = ex2_approx(fmaf(s[64 + 2 * j + 1], sl2, -mu));
-          ls[j & 1] += p0 + p1;
-          ls[2 + (j & 1)] += p2 + p3;
-          pk0[j] = pack_bf16x2(p0, p1);
-          pk1[j] = pack_bf16x2(p2, p3);
+        for (int j = 0; j < 64; ++j) {
+          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
+                                     sc2, nm2);
+          float x0, x1;
+          f2_unpack(x2, x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          sum2[j & 3] = f2_add(sum2[j & 3], f2_pack(p0, p1));
+          pk[j] = pack_bf16x2(p0, p1);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        tmem_st32(tS + 64, pk0);
-        tmem_st32(tS + 96, pk1);
+        tmem_st64(tS + 64, pk);
+        {
+          float a0, a1, b0, b1, c0, c1, d0, d1;
+          f2_unpack(f2_add(sum2[0], sum2[1]), a0, a1);
+          f2_unpack(f2_add(sum2[2], sum2[3]), b0, b1);
+          (void)c0; (void)c1; (void)d0; (void)d1;
+          l += (a0 + a1) + (b0 + b1);
+        }
         if (has_pv && __any_sync(0xffffffffu, need)) {
           uint32_t rr[32];
 #pragma unroll
