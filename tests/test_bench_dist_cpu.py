@@ -1,0 +1,54 @@
+"""The benchmark's multi-rank path on CPU: two gloo ranks under torchrun agree on
+the maximum of their timed regions (the value every rank reports), with the
+barrier around it."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def test_dist_max_two_gloo_ranks(tmp_path):
+    pytest.importorskip("torch.distributed")
+    script = tmp_path / "ranks.py"
+    script.write_text(
+        "import json, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import torch\n"
+        "import bench\n"
+        "world, rank, local = bench.dist_setup()\n"
+        "bench.dist_barrier(world)\n"
+        "m = bench.dist_max(float(10 * rank + 3), world)\n"
+        "bench.dist_barrier(world)\n"
+        "print('RESULT ' + json.dumps({'rank': rank, 'world': world, 'max': m}), flush=True)\n"
+        "torch.distributed.destroy_process_group()\n")
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", MASTER_ADDR="127.0.0.1")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), str(script)]
+    out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=240)
+    assert out.returncode == 0, out.stderr[-2000:]
+    res = [json.loads(line.split("RESULT ", 1)[1]) for line in out.stdout.splitlines()
+           if "RESULT " in line]
+    assert sorted(r["rank"] for r in res) == [0, 1]
+    assert all(r["world"] == 2 and r["max"] == 13.0 for r in res)
+
+
+def test_valid_pair_count_closed_form():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    cu = np.array([0, 100, 256])
+    assert bench.valid_pairs(cu, True) == 100 * 101 // 2 + 156 * 157 // 2
+    assert bench.valid_pairs(cu, False) == 100 * 100 + 156 * 156
