@@ -9,8 +9,10 @@
 // causal (HSAP abstract: no cross-contamination of packed documents).
 //
 // Roles (12 warps):
-//   warp 0      TMA producer: Q tiles once per unit, K and V tiles into a
-//               2-stage ring (128-byte swizzled, as the MMA reads them).
+//   warp 0      TMA producer: Q tiles once per unit, K tiles into a 2-stage and
+//               V tiles into a 3-stage ring (128-byte swizzled, as the MMA
+//               reads them); it walks the tiles and publishes one record per K
+//               stage (tile classes, last-of-unit).
 //   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma.
 //   warps 4-7   softmax for Q tile 0 (rows 0-127 of the unit).
 //   warps 8-11  softmax for Q tile 1 (rows 128-255).
@@ -36,19 +38,29 @@ namespace {
 
 constexpr int CLS_SKIP = 0, CLS_MASKED = 1, CLS_FULL = 2;
 
+// Tile record the producer publishes with each K stage, so that the MMA lane
+// does no tile bookkeeping of its own: bits [0,2) class of Q tile 0, [2,4)
+// class of Q tile 1, REC_TILE when K/V were loaded, REC_LAST on the unit's last
+// record (a unit without tiles publishes one record with REC_LAST only).
+constexpr int REC_TILE = 16, REC_LAST = 32;
+
 template <int D>
 struct Cfg {
-  static constexpr int NSTAGE = 2;
+  // K is consumed by the first MMA of a tile and V by the last, so V buffers
+  // are held longer: the V ring is one stage deeper than the K ring.
+  static constexpr int KSTAGE = 2;
+  static constexpr int VSTAGE = 3;
   static constexpr int KSUB = D / 64;             // 128-byte sub-tiles along d
   static constexpr int SUB_BYTES = 128 * 128;     // [128 rows][64 bf16]
   static constexpr int TILE_BYTES = KSUB * SUB_BYTES;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + NSTAGE * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NSTAGE * TILE_BYTES;
-  static constexpr int N_BARS = 17;
-  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
-  static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_V = OFF_K + KSTAGE * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VSTAGE * TILE_BYTES;
+  static constexpr int N_BARS = 16;
+  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;   // TMEM address, abort flag
+  static constexpr int OFF_REC = OFF_MISC + 8;             // one tile record per K stage
+  static constexpr int SMEM_ALLOC = OFF_REC + 4 * KSTAGE + 1024;
   static constexpr int TM_S = 0;
   static constexpr int TM_O = 256;
   static constexpr int TMEM_COLS = 512;
@@ -56,10 +68,11 @@ struct Cfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);
 };
 
-// Barrier slots.
+// Barrier slots. KV_FULL[s] completes when both the K tile of K stage s and
+// the V tile loaded with it have landed (one wait per tile for the MMA lane).
 enum {
-  B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = 4, B_V_FULL = 6, B_V_EMPTY = 8,
-  B_S_FULL = 10, B_P_FULL = 12, B_O_FULL = 14, B_DRAIN = 16
+  B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_K_EMPTY = 4, B_V_EMPTY = 6,
+  B_S_FULL = 9, B_P_FULL = 11, B_O_FULL = 13, B_DRAIN = 15
 };
 
 struct QTile {
@@ -123,6 +136,54 @@ __device__ __forceinline__ bool next_tile(const AttnArgs& a, Cursor& c, const QT
   }
 }
 
+// Non-blocking barrier tests run by the MMA lane just before the last MMA of a
+// group, while that group is still executing: the MMA queue is shallow, so a
+// test or wait between groups would leave the tensor core idle.
+struct Probe {
+  uint32_t bar, par;
+  int on;
+};
+
+__device__ __forceinline__ int run_probes(const Probe& a, const Probe& b) {
+  int r = 0;
+  if (a.on && mbar_test(a.bar, a.par)) r |= 1;
+  if (b.on && mbar_test(b.bar, b.par)) r |= 2;
+  return r;
+}
+
+// S = Q K^T for one Q tile: D/16 MMAs of 128x128x16. Descriptor bases are
+// fixed; only the 14-bit start address field (16-byte units) advances.
+template <int D>
+__device__ __forceinline__ int mma_qk(uint32_t d_t, uint64_t a0, uint64_t b0, const Probe& pa,
+                                      const Probe& pb) {
+  using C = Cfg<D>;
+  int res = 0;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    if (kk == D / 16 - 1) res = run_probes(pa, pb);
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::SUB_BYTES + (kk & 3) * 32) >> 4);
+    tc_mma_ss(d_t, a0 + off, b0 + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
+  }
+  return res;
+}
+
+// Half h of O += P V: keys 64h .. 64h+63 (K steps 4h .. 4h+3); P read from
+// tensor memory, V from shared memory (MN-major).
+template <int D>
+__device__ __forceinline__ int mma_pv_half(uint32_t d_t, uint32_t a_t, uint64_t b0, int h, int acc,
+                                           const Probe& pa, const Probe& pb) {
+  using C = Cfg<D>;
+  int res = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int kk = 4 * h + q;
+    if (q == 3) res = run_probes(pa, pb);
+    tc_mma_ts(d_t, a_t + 8 * kk, b0 + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV,
+              (acc || kk > 0) ? 1u : 0u);
+  }
+  return res;
+}
+
 template <int D, int OUT_FP32>
 __global__ void __launch_bounds__(384, 1)
 attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
@@ -137,6 +198,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* rec = reinterpret_cast<volatile int*>(smem + C::OFF_REC);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -144,15 +206,14 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q_FULL), 1);
     mbar_init(bar(B_Q_EMPTY), 1);
-    for (int s = 0; s < C::NSTAGE; ++s) {
-      mbar_init(bar(B_K_FULL + s), 1);
+    for (int s = 0; s < C::KSTAGE; ++s) {
+      mbar_init(bar(B_KV_FULL + s), 1);
       mbar_init(bar(B_K_EMPTY + s), 1);
-      mbar_init(bar(B_V_FULL + s), 1);
-      mbar_init(bar(B_V_EMPTY + s), 1);
     }
+    for (int s = 0; s < C::VSTAGE; ++s) mbar_init(bar(B_V_EMPTY + s), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_S_FULL + i), 1);
-      mbar_init(bar(B_P_FULL + i), 4);
+      mbar_init(bar(B_P_FULL + i), 4);   // P_i stored (and O_i rescaled)
       mbar_init(bar(B_O_FULL + i), 1);
     }
     mbar_init(bar(B_DRAIN), 1);
@@ -173,10 +234,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const unsigned long long tmo = a.timeout_ns;
 
   // Register split: the producer/MMA warpgroup needs few registers, the two
-  // softmax warpgroups hold a 128-column row of S each. 128*104 + 256*200 equals
+  // softmax warpgroups hold a 128-column row of S each. 128*136 + 256*184 equals
   // the 384*168 the block is launched with.
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 136;");
   }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -184,9 +245,11 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      uint32_t kv_cnt = 0, unit_cnt = 0;
-      int armed_k[C::NSTAGE] = {}, armed_v[C::NSTAGE] = {};
-      uint32_t par_k[C::NSTAGE] = {}, par_v[C::NSTAGE] = {};
+      uint32_t unit_cnt = 0;
+      int kst = 0, vst = 0;
+      uint32_t kph = 0, vph = 0;
+      int armed_k[C::KSTAGE] = {};
+      uint32_t par_k[C::KSTAGE] = {};
       int armed_q = 0;
       uint32_t par_q = 0;
       bool ok = true;
@@ -202,26 +265,38 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           for (int s = 0; s < C::KSUB; ++s)
             tma_load_3d(sQ + i * C::TILE_BYTES + s * C::SUB_BYTES, &tmq, bar(B_Q_FULL), 64 * s,
                         ui.h, ui.q0 + 128 * i);
+        // The tile walk runs one tile ahead so that each record can say
+        // whether it is the unit's last.
         Cursor cur{ui.item_lo, ui.item_hi, 0, 0};
-        int ka, kb, cls[2];
-        while (next_tile(a, cur, qt, ka, kb, cls)) {
-          const int st = kv_cnt % C::NSTAGE;
-          const uint32_t ph = (kv_cnt / C::NSTAGE) & 1;
-          if (!mbar_wait_bounded(bar(B_K_EMPTY + st), ph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(B_K_FULL + st), C::TILE_BYTES);
-          armed_k[st] = 1;
-          par_k[st] = ph;
+        int ka = 0, kb = 0, cls[2] = {0, 0};
+        bool have = next_tile(a, cur, qt, ka, kb, cls);
+        if (!have) {
+          if (!mbar_wait_bounded(bar(B_K_EMPTY + kst), kph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
+          rec[kst] = REC_LAST;
+          mbar_arrive(bar(B_KV_FULL + kst));
+          if (++kst == C::KSTAGE) { kst = 0; kph ^= 1; }
+        }
+        while (have) {
+          int nka, nkb, ncls[2];
+          const bool nxt = next_tile(a, cur, qt, nka, nkb, ncls);
+          if (!mbar_wait_bounded(bar(B_K_EMPTY + kst), kph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_bounded(bar(B_V_EMPTY + vst), vph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
+          rec[kst] = REC_TILE | cls[0] | (cls[1] << 2) | (nxt ? 0 : REC_LAST);
+          const uint32_t full = bar(B_KV_FULL + kst);
+          mbar_arrive_expect_tx(full, 2 * C::TILE_BYTES);
+          armed_k[kst] = 1;
+          par_k[kst] = kph;
           for (int s = 0; s < C::KSUB; ++s)
-            tma_load_3d(sK + st * C::TILE_BYTES + s * C::SUB_BYTES, &tmk, bar(B_K_FULL + st), 64 * s,
-                        hk, ka);
-          if (!mbar_wait_bounded(bar(B_V_EMPTY + st), ph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(B_V_FULL + st), C::TILE_BYTES);
-          armed_v[st] = 1;
-          par_v[st] = ph;
+            tma_load_3d(sK + kst * C::TILE_BYTES + s * C::SUB_BYTES, &tmk, full, 64 * s, hk, ka);
           for (int s = 0; s < C::KSUB; ++s)
-            tma_load_3d(sV + st * C::TILE_BYTES + s * C::SUB_BYTES, &tmv, bar(B_V_FULL + st), 64 * s,
-                        hk, ka);
-          ++kv_cnt;
+            tma_load_3d(sV + vst * C::TILE_BYTES + s * C::SUB_BYTES, &tmv, full, 64 * s, hk, ka);
+          if (++kst == C::KSTAGE) { kst = 0; kph ^= 1; }
+          if (++vst == C::VSTAGE) { vst = 0; vph ^= 1; }
+          ka = nka;
+          kb = nkb;
+          cls[0] = ncls[0];
+          cls[1] = ncls[1];
+          have = nxt;
         }
       }
       if (!ok) {
@@ -229,10 +304,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         volatile int no_abort = 0;
         const unsigned long long drain = 50000000ull;
         if (armed_q) mbar_wait_bounded(bar(B_Q_FULL), par_q, drain, a.err, &no_abort);
-        for (int s = 0; s < C::NSTAGE; ++s) {
-          if (armed_k[s]) mbar_wait_bounded(bar(B_K_FULL + s), par_k[s], drain, a.err, &no_abort);
-          if (armed_v[s]) mbar_wait_bounded(bar(B_V_FULL + s), par_v[s], drain, a.err, &no_abort);
-        }
+        for (int s = 0; s < C::KSTAGE; ++s)
+          if (armed_k[s]) mbar_wait_bounded(bar(B_KV_FULL + s), par_k[s], drain, a.err, &no_abort);
       }
     }
     __syncwarp();
@@ -243,87 +316,88 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       const uint64_t dq1 = smem_desc_sw128(sQ + C::TILE_BYTES, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sV, C::SUB_BYTES, 1024);
-      uint32_t kv_cnt = 0, unit_cnt = 0, pcnt0 = 0, pcnt1 = 0;
+      uint32_t unit_cnt = 0, pcnt0 = 0, pcnt1 = 0;
+      int kst = 0, vst = 0;
+      uint32_t kph = 0;
       bool ok = true;
+      const Probe none{0u, 0u, 0};
+      const uint32_t dS0 = tmem + C::TM_S, dS1 = tmem + C::TM_S + 128;
+      const uint32_t dO0 = tmem + C::TM_O, dO1 = tmem + C::TM_O + D;
+      const uint32_t aP0 = dS0 + 64, aP1 = dS1 + 64;
+      const uint64_t kstep = C::TILE_BYTES >> 4;
+
+      bool rdy_k = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
-        const UnitInfo ui = unit_info(a, u);
-        const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
         if (!mbar_wait_bounded(bar(B_Q_FULL), unit_cnt & 1, tmo, a.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
         int has_pv0 = 0, has_pv1 = 0;
-        int have_prev = 0, prev_st = 0, prev_cls1 = 0;
-        Cursor cur{ui.item_lo, ui.item_hi, 0, 0};
-        int ka, kb, cls[2];
-
-        // Descriptor bases are computed once; per MMA only the 14-bit start
-        // address field (bits [0,14), in 16-byte units) advances, by one add.
-        auto issue_qk = [&](int i, int st) {
-          const uint32_t d_t = tmem + C::TM_S + 128 * i;
-          const uint64_t a0 = i ? dq1 : dq0;
-          const uint64_t b0 = dk0 + static_cast<uint64_t>(st * (C::TILE_BYTES >> 4));
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::SUB_BYTES + (kk & 3) * 32) >> 4);
-            tc_mma_ss(d_t, a0 + off, b0 + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
-          }
-        };
-        auto issue_pv = [&](int i, int st, int acc) {
-          const uint32_t d_t = tmem + C::TM_O + D * i;
-          const uint32_t a_t = tmem + C::TM_S + 128 * i + 64;
-          const uint64_t b0 = dv0 + static_cast<uint64_t>(st * (C::TILE_BYTES >> 4));
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc_mma_ts(d_t, a_t + 8 * kk, b0 + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV,
-                      (acc || kk > 0) ? 1u : 0u);
-        };
-
-        while (next_tile(a, cur, qt, ka, kb, cls)) {
-          const int st = kv_cnt % C::NSTAGE;
-          const uint32_t ph = (kv_cnt / C::NSTAGE) & 1;
-          if (!mbar_wait_bounded(bar(B_K_FULL + st), ph, tmo, a.err, abort_flag)) { ok = false; break; }
+        int have_prev = 0, prev_vs = 0, prev_c1 = 0;
+        while (true) {
+          if (!rdy_k && !mbar_wait_bounded(bar(B_KV_FULL + kst), kph, tmo, a.err, abort_flag)) { ok = false; break; }
+          rdy_k = false;
           tc_fence_after();
-          if (cls[0] != CLS_SKIP) {
-            issue_qk(0, st);
-            tc_commit(bar(B_S_FULL + 0));
-          }
-          if (have_prev) {
-            if (prev_cls1 != CLS_SKIP) {
-              if (!mbar_wait_bounded(bar(B_P_FULL + 1), pcnt1 & 1, tmo, a.err, abort_flag)) { ok = false; break; }
-              ++pcnt1;
+          const int r = rec[kst];
+          const int nkst = (kst + 1 == C::KSTAGE) ? 0 : kst + 1;
+          const uint32_t nkph = (kst + 1 == C::KSTAGE) ? (kph ^ 1) : kph;
+          if (r & REC_TILE) {
+            const int c0 = r & 3, c1 = (r >> 2) & 3;
+            const int pv1 = have_prev && prev_c1 != CLS_SKIP;
+            const uint64_t bK = dk0 + static_cast<uint64_t>(kst) * kstep;
+            const uint64_t bV = dv0 + static_cast<uint64_t>(vst) * kstep;
+            const uint64_t bVp = dv0 + static_cast<uint64_t>(prev_vs) * kstep;
+            const Probe p1{bar(B_P_FULL + 1), pcnt1 & 1, pv1};
+            const Probe p0{bar(B_P_FULL + 0), pcnt0 & 1, c0 != CLS_SKIP};
+            const Probe pk{bar(B_KV_FULL + nkst), nkph, 1};
+            int got1 = 0, got0 = 0;
+            if (c0 != CLS_SKIP) {
+              got1 = mma_qk<D>(dS0, dq0, bK, p1, none) & 1;
+              tc_commit(bar(B_S_FULL + 0));
+            }
+            if (pv1) {
+              if (!got1 && !mbar_wait_bounded(p1.bar, p1.par, tmo, a.err, abort_flag)) { ok = false; break; }
               tc_fence_after();
-              issue_pv(1, prev_st, has_pv1);
+              mma_pv_half<D>(dO1, aP1, bVp, 0, has_pv1, none, none);
+              got0 = mma_pv_half<D>(dO1, aP1, bVp, 1, 1, p0, none) & 1;
+              ++pcnt1;
               has_pv1 = 1;
             }
-            tc_commit(bar(B_V_EMPTY + prev_st));
+            if (have_prev) tc_commit(bar(B_V_EMPTY + prev_vs));
+            if (c1 != CLS_SKIP) {
+              const int g = mma_qk<D>(dS1, dq1, bK, got0 ? none : p0, none);
+              got0 |= g & 1;
+              tc_commit(bar(B_S_FULL + 1));
+            }
+            tc_commit(bar(B_K_EMPTY + kst));
+            if (c0 != CLS_SKIP) {
+              if (!got0 && !mbar_wait_bounded(p0.bar, p0.par, tmo, a.err, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              mma_pv_half<D>(dO0, aP0, bV, 0, has_pv0, none, none);
+              rdy_k = mma_pv_half<D>(dO0, aP0, bV, 1, 1, (r & REC_LAST) ? none : pk, none) & 1;
+              ++pcnt0;
+              has_pv0 = 1;
+            }
+            have_prev = 1;
+            prev_vs = vst;
+            prev_c1 = c1;
+            if (++vst == C::VSTAGE) vst = 0;
+          } else {
+            tc_commit(bar(B_K_EMPTY + kst));  // nothing was loaded: hand the slot back
           }
-          if (cls[1] != CLS_SKIP) {
-            issue_qk(1, st);
-            tc_commit(bar(B_S_FULL + 1));
-          }
-          tc_commit(bar(B_K_EMPTY + st));
-          if (!mbar_wait_bounded(bar(B_V_FULL + st), ph, tmo, a.err, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          if (cls[0] != CLS_SKIP) {
-            if (!mbar_wait_bounded(bar(B_P_FULL + 0), pcnt0 & 1, tmo, a.err, abort_flag)) { ok = false; break; }
-            ++pcnt0;
-            tc_fence_after();
-            issue_pv(0, st, has_pv0);
-            has_pv0 = 1;
-          }
-          have_prev = 1;
-          prev_st = st;
-          prev_cls1 = cls[1];
-          ++kv_cnt;
+          kst = nkst;
+          kph = nkph;
+          if (r & REC_LAST) break;
         }
         if (!ok) break;
         if (have_prev) {
-          if (prev_cls1 != CLS_SKIP) {
+          if (prev_c1 != CLS_SKIP) {
+            const uint64_t bVp = dv0 + static_cast<uint64_t>(prev_vs) * kstep;
             if (!mbar_wait_bounded(bar(B_P_FULL + 1), pcnt1 & 1, tmo, a.err, abort_flag)) { ok = false; break; }
-            ++pcnt1;
             tc_fence_after();
-            issue_pv(1, prev_st, has_pv1);
+            mma_pv_half<D>(dO1, aP1, bVp, 0, has_pv1, none, none);
+            mma_pv_half<D>(dO1, aP1, bVp, 1, 1, none, none);
+            ++pcnt1;
           }
-          tc_commit(bar(B_V_EMPTY + prev_st));
+          tc_commit(bar(B_V_EMPTY + prev_vs));
         }
         tc_commit(bar(B_Q_EMPTY));
         tc_commit(bar(B_O_FULL + 0));
@@ -337,7 +411,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
     const int wg = (warp - 4) >> 2;       // which Q tile
     const int wq = warp & 3;              // tensor-memory lane quarter
     const int r = wq * 32 + lane;         // row within the Q tile
@@ -403,40 +477,47 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           m = m_new;
         }
         const float mu = (m == NEG_INF) ? 0.f : m;
+        const bool rescale = has_pv && __any_sync(0xffffffffu, need);
         // p = 2^(s * scale * log2 e - m): packed FMA, then MUFU ex2, packed
-        // row-sum, bf16 pairs written back over columns [64, 128) of S.
+        // row-sum; bf16 pairs are written back over columns [64, 128) of S,
+        // in two halves to keep fewer registers live.
         const uint64_t sc2 = f2_pack(sl2, sl2);
         const uint64_t nm2 = f2_pack(-mu, -mu);
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[64];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
-                                     sc2, nm2);
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          sum2[j & 3] = f2_add(sum2[j & 3], f2_pack(p0, p1));
-          pk[j] = pack_bf16x2(p0, p1);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c2 = 64 * hh + 2 * j;
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[c2]), __uint_as_float(sr[c2 + 1])),
+                                       sc2, nm2);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            sum2[j & 3] = f2_add(sum2[j & 3], f2_pack(p0, p1));
+            pk[j] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + 64 + 32 * hh, pk);
+          if (hh == 0 && rescale) {
+            // O_i rescale (rare: the row maximum grew by more than 2^8); it
+            // must be done before P_i V is allowed to start.
+            uint32_t rr[32];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              tmem_ld32_sync(tO + 32 * ch, rr);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+              tmem_st32(tO + 32 * ch, rr);
+            }
+          }
         }
-        tmem_st64(tS + 64, pk);
         {
-          float a0, a1, b0, b1, c0, c1, d0, d1;
+          float a0, a1, b0, b1;
           f2_unpack(f2_add(sum2[0], sum2[1]), a0, a1);
           f2_unpack(f2_add(sum2[2], sum2[3]), b0, b1);
-          (void)c0; (void)c1; (void)d0; (void)d1;
           l += (a0 + a1) + (b0 + b1);
-        }
-        if (has_pv && __any_sync(0xffffffffu, need)) {
-          uint32_t rr[32];
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            tmem_ld32_sync(tO + 32 * ch, rr);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
-            tmem_st32(tO + 32 * ch, rr);
-          }
         }
         tmem_wait_st();
         tc_fence_before();

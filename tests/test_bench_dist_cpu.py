@@ -32,15 +32,15 @@ def test_dist_max_two_gloo_ranks(tmp_path):
         "bench.dist_barrier(world)\n"
         "m = bench.dist_max(float(10 * rank + 3), world)\n"
         "bench.dist_barrier(world)\n"
-        "print('RESULT ' + json.dumps({'rank': rank, 'world': world, 'max': m}), flush=True)\n"
+        f"open({str(tmp_path)!r} + f'/rank{{rank}}.json', 'w').write("
+        "json.dumps({'rank': rank, 'world': world, 'max': m}))\n"
         "torch.distributed.destroy_process_group()\n")
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="", MASTER_ADDR="127.0.0.1")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), str(script)]
     out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=240)
     assert out.returncode == 0, out.stderr[-2000:]
-    res = [json.loads(line.split("RESULT ", 1)[1]) for line in out.stdout.splitlines()
-           if "RESULT " in line]
+    res = [json.loads((tmp_path / f"rank{r}.json").read_text()) for r in (0, 1)]
     assert sorted(r["rank"] for r in res) == [0, 1]
     assert all(r["world"] == 2 and r["max"] == 13.0 for r in res)
 
