@@ -57,10 +57,11 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KSTAGE * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + VSTAGE * TILE_BYTES;
-  static constexpr int N_BARS = 16;
+  static constexpr int N_BARS = 20;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;   // TMEM address, abort flag
   static constexpr int OFF_REC = OFF_MISC + 8;             // one tile record per K stage
-  static constexpr int SMEM_ALLOC = OFF_REC + 4 * KSTAGE + 1024;
+  static constexpr int OFF_URING = OFF_REC + 4 * KSTAGE;   // two unit ids in flight
+  static constexpr int SMEM_ALLOC = OFF_URING + 8 + 1024;
   static constexpr int TM_S = 0;
   static constexpr int TM_O = 256;
   static constexpr int TMEM_COLS = 512;
@@ -72,8 +73,13 @@ struct Cfg {
 // the V tile loaded with it have landed (one wait per tile for the MMA lane).
 enum {
   B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_K_EMPTY = 4, B_V_EMPTY = 6,
-  B_S_FULL = 9, B_P_FULL = 11, B_O_FULL = 13, B_DRAIN = 15
+  B_S_FULL = 9, B_P_FULL = 11, B_O_FULL = 13, B_DRAIN = 15, B_U_FULL = 16, B_U_EMPTY = 18
 };
+
+// Units reach the MMA lane and the softmax warps through a two-slot ring filled
+// by the producer lane: one consumer arrival from the MMA lane and one per
+// softmax warp frees a slot.
+constexpr int UNIT_CONSUMERS = 9;
 
 struct QTile {
   int qa, qb;   // valid rows [qa, qb) (empty when qa >= qb)
@@ -199,6 +205,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* rec = reinterpret_cast<volatile int*>(smem + C::OFF_REC);
+  volatile int* uring = reinterpret_cast<volatile int*>(smem + C::OFF_URING);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -217,6 +224,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       mbar_init(bar(B_O_FULL + i), 1);
     }
     mbar_init(bar(B_DRAIN), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_U_FULL + i), 1);
+      mbar_init(bar(B_U_EMPTY + i), UNIT_CONSUMERS);
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -253,7 +264,30 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       int armed_q = 0;
       uint32_t par_q = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+      // Work units: claimed from the dynamic queue (largest groups first, so
+      // the tail is made of small units) or strided over the CTAs.
+      int k_static = 0;
+      auto fetch = [&]() -> int {
+        int v;
+        if (a.work_counter) {
+          v = atomicAdd(a.work_counter, 1);
+        } else {
+          v = static_cast<int>(blockIdx.x) + k_static * static_cast<int>(gridDim.x);
+          ++k_static;
+        }
+        return v < n_units ? v : -1;
+      };
+      int uslot = 0;
+      uint32_t uph = 0;
+      int u_next = fetch();
+      for (;; ++unit_cnt) {
+        const int u = u_next;
+        if (!mbar_wait_bounded(bar(B_U_EMPTY + uslot), uph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
+        uring[uslot] = u;
+        mbar_arrive(bar(B_U_FULL + uslot));
+        if (++uslot == 2) { uslot = 0; uph ^= 1; }
+        if (u < 0) break;
+        u_next = fetch();
         const UnitInfo ui = unit_info(a, u);
         const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
         const int hk = ui.h / G;
@@ -298,6 +332,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           cls[1] = ncls[1];
           have = nxt;
         }
+        if (!ok) break;
       }
       if (!ok) {
         // Aborting: let every copy already issued land before the block exits.
@@ -327,7 +362,14 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       const uint64_t kstep = C::TILE_BYTES >> 4;
 
       bool rdy_k = false;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+      int uslot = 0;
+      uint32_t uph = 0;
+      for (;; ++unit_cnt) {
+        if (!mbar_wait_bounded(bar(B_U_FULL + uslot), uph, tmo, a.err, abort_flag)) { ok = false; break; }
+        const int u = uring[uslot];
+        mbar_arrive(bar(B_U_EMPTY + uslot));
+        if (++uslot == 2) { uslot = 0; uph ^= 1; }
+        if (u < 0) break;
         if (!mbar_wait_bounded(bar(B_Q_FULL), unit_cnt & 1, tmo, a.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
         int has_pv0 = 0, has_pv1 = 0;
@@ -422,7 +464,15 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     const float NEG_INF = -__int_as_float(0x7f800000);
     uint32_t s_cnt = 0, unit_cnt = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+    int uslot = 0;
+    uint32_t uph = 0;
+    for (;; ++unit_cnt) {
+      if (!mbar_wait_bounded(bar(B_U_FULL + uslot), uph, tmo, a.err, abort_flag)) { ok = false; break; }
+      const int u = uring[uslot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_U_EMPTY + uslot));
+      if (++uslot == 2) { uslot = 0; uph ^= 1; }
+      if (u < 0) break;
       const UnitInfo ui = unit_info(a, u);
       const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
       const QTile my = wg ? qt[1] : qt[0];

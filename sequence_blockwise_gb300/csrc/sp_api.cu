@@ -223,6 +223,7 @@ sp_status sp_packed_attention(const void* q, const void* k, const void* v, void*
   const sp::WsLayout L = sp::ws_layout(n_items);
   a.items = items_dev;
   a.header = static_cast<const int32_t*>(workspace);
+  a.work_counter = static_cast<int32_t*>(workspace) + sp::WS_COUNTER;
   a.segs = reinterpret_cast<const sp::SegEntry*>(static_cast<const char*>(workspace) + L.off_segs);
   a.rows_per_unit = rpu;
   a.out_mode = 0;

@@ -133,6 +133,7 @@ prep_kernel(const sp_item* __restrict__ items, int n, int T, int Hq, int rpu, in
     header[WS_N_SEGS] = fail ? 0 : nseg;
     header[WS_N_UNITS] = fail ? 0 : static_cast<int32_t>(total);
     header[WS_STATUS] = fail ? 1 : 0;
+    header[WS_COUNTER] = 0;
     if (fail) atomicOr(err, ERR_INTERNAL_BIT);
   }
 }

@@ -25,7 +25,8 @@ struct SegEntry {
 static_assert(sizeof(SegEntry) == 32, "SegEntry is 32 bytes");
 
 // Workspace header (int32 words).
-enum : int { WS_N_SEGS = 0, WS_N_UNITS = 1, WS_STATUS = 2, WS_HEADER_WORDS = 16 };
+// WS_COUNTER: next work unit to hand out (reset to 0 by the set-up kernel).
+enum : int { WS_N_SEGS = 0, WS_N_UNITS = 1, WS_STATUS = 2, WS_COUNTER = 3, WS_HEADER_WORDS = 16 };
 
 struct AttnArgs {
   const void* q;
@@ -44,6 +45,7 @@ struct AttnArgs {
   const sp_item* items;
   const SegEntry* segs;
   const int32_t* header;
+  int32_t* work_counter;  // dynamic unit queue (nullptr: static striding over CTAs)
   sp_item inline_item;
   SegEntry inline_seg;
   int32_t inline_n_units;
