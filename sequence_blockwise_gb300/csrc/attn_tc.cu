@@ -117,7 +117,25 @@ __device__ __forceinline__ int classify(const QTile& t, int ka, int kb, int caus
 
 struct Cursor {
   int item, item_end, kv_e, k0;
+  int lo, hi;  // keys any row of the unit may attend: [lo, hi)
 };
+
+// Cursor over a unit's items. Each item's key range is first clipped to the
+// keys some row of the unit may attend (the documents of its rows, and keys
+// up to its last row when causal), so that no tile is visited for keys that
+// are masked for every row; tiles start at the clipped start.
+__device__ __forceinline__ Cursor make_cursor(const UnitInfo& ui, const QTile (&qt)[2], int causal) {
+  Cursor c{ui.item_lo, ui.item_hi, 0, 0, 0, 0};
+  const bool e0 = qt[0].qa < qt[0].qb, e1 = qt[1].qa < qt[1].qb;
+  if (!e0 && !e1) {
+    c.item = c.item_end;  // no valid row: no tile
+    return c;
+  }
+  c.lo = e0 ? qt[0].ds : qt[1].ds;
+  c.hi = e1 ? qt[1].de : qt[0].de;
+  if (causal) c.hi = min(c.hi, (e1 ? qt[1].qb : qt[0].qb));
+  return c;
+}
 
 // Advances to the next 128-key tile of the unit that is not SKIP for both Q
 // tiles. Every role runs this same function, so all agree on the sequence.
@@ -129,8 +147,8 @@ __device__ __forceinline__ bool next_tile(const AttnArgs& a, Cursor& c, const QT
       int b, e;
       item_range(a, c.item, b, e);
       ++c.item;
-      c.k0 = b;
-      c.kv_e = e;
+      c.k0 = max(b, c.lo);
+      c.kv_e = min(e, c.hi);
       continue;
     }
     ka = c.k0;
@@ -301,7 +319,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
                         ui.h, ui.q0 + 128 * i);
         // The tile walk runs one tile ahead so that each record can say
         // whether it is the unit's last.
-        Cursor cur{ui.item_lo, ui.item_hi, 0, 0};
+        Cursor cur = make_cursor(ui, qt, a.causal);
         int ka = 0, kb = 0, cls[2] = {0, 0};
         bool have = next_tile(a, cur, qt, ka, kb, cls);
         if (!have) {
@@ -487,7 +505,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       const int rcausal_end = a.causal ? t + 1 : 0x7fffffff;
       float m = NEG_INF, l = 0.f;
       int has_pv = 0;
-      Cursor cur{ui.item_lo, ui.item_hi, 0, 0};
+      Cursor cur = make_cursor(ui, qt, a.causal);
       int ka, kb, cls[2];
       while (next_tile(a, cur, qt, ka, kb, cls)) {
         const int c = wg ? cls[1] : cls[0];
