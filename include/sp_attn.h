@@ -108,6 +108,29 @@ sp_status sp_schedule_build(sp_sched_kind kind, int32_t P, int32_t total_tokens,
  * nothing. Same errors as the TASP schedule. Results are cached per (P, seed). */
 sp_status sp_tasp_cycles(int32_t P, uint64_t seed, int32_t* out_succ);
 
+/* sp_schedule_link_bytes — host only; the communication volume a schedule
+ * implies on the virtual ranks' links ("TASP: Topology-aware Sequence
+ * Parallelism", abstract: a Ring AllGather is P-1 iterations of ring transfers
+ * that use only one ring of links; TASP decomposes the complete digraph into
+ * P-1 Hamiltonian rings and moves one piece of every chunk on each ring in
+ * every iteration).
+ *  out[(t-1)*P*P + u*P + v] = bytes sent over the directed link u -> v in
+ *  transfer iteration t = 1 .. P-1:
+ *   RING:   rank r receives from r-1 the chunk that started at rank r-t;
+ *   ZIGZAG: the same ring, carrying both chunks of rank r-t;
+ *   TASP:   on ring c, rank r receives from its predecessor on c piece c of the
+ *           chunk that started t hops upstream on c.
+ *  A block of keys costs (kv_end - kv_begin) * bytes_per_token.
+ *  needed_only != 0: a block stops travelling after the last rank on its ring
+ *  that needs it (a query with a valid key in the block; sequence-aware
+ *  pruning, HSAP abstract); otherwise the full AllGather is counted.
+ *  out: caller-allocated int64 [(P-1)*P*P] (unused when P == 1).
+ *  Errors as sp_schedule_build. */
+sp_status sp_schedule_link_bytes(sp_sched_kind kind, int32_t P, int32_t total_tokens,
+                                 const int32_t* cu_seqlens_host, int32_t ndocs, int32_t causal,
+                                 uint64_t seed, int64_t bytes_per_token, int32_t needed_only,
+                                 int64_t* out);
+
 /* sp_partial_attn — one partial attention step ("partial attention
  * computation", HSAP abstract; one iteration of Ring Attention, TASP abstract).
  * For every query row t in [q_begin, q_end) and head h, over the keys

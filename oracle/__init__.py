@@ -64,6 +64,10 @@ def _load():
         lib.oracle_check_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
                                               ctypes.c_int, ctypes.c_int, i32p, ctypes.c_longlong,
                                               i32p, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
+        lib.oracle_link_bytes.restype = ctypes.c_int
+        lib.oracle_link_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                          ctypes.c_int, i32p, ctypes.c_longlong, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_longlong)]
         lib.oracle_check_cu_seqlens.restype = ctypes.c_int
         lib.oracle_check_cu_seqlens.argtypes = [i32p, ctypes.c_int, ctypes.c_int]
         lib.oracle_doc_of.restype = ctypes.c_int
@@ -200,3 +204,19 @@ def check_schedule(kind: int, P: int, T: int, cu_seqlens, causal: bool, items, s
     rc = lib.oracle_check_schedule(kind, P, T, cup, len(cu) - 1, int(causal), itp, len(it), scp,
                                    int(brute), buf, 256)
     return int(rc), buf.value.decode()
+
+
+def link_bytes(kind: int, P: int, T: int, cu_seqlens, causal: bool, succ=None,
+               bytes_per_token: int = 1, needed_only: bool = False):
+    """Bytes per directed link per AllGather iteration, int64 [P-1, P, P] (src, dst)."""
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    if succ is None:
+        succ = np.zeros((max(P - 1, 1), max(P, 1)), dtype=np.int32)
+    sc, scp = _i32(succ)
+    out = np.zeros((max(P - 1, 1), P, P), dtype=np.int64)
+    rc = lib.oracle_link_bytes(kind, P, T, cup, len(cu) - 1, int(causal), scp, int(bytes_per_token),
+                               int(needed_only), out.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)))
+    if rc != 0:
+        raise ValueError(f"oracle_link_bytes rejected its arguments (code {rc})")
+    return out[:max(P - 1, 0)]

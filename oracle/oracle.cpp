@@ -418,4 +418,93 @@ int oracle_check_schedule(int kind, int P, int T, const int32_t* cu, int ndocs, 
   return 0;
 }
 
+// Communication model of a schedule, stated from the receiving side: in
+// iteration t (1..P-1) of the AllGather, what does each rank receive and from
+// whom (TASP abstract: Ring AllGather = P-1 iterations of ring transfers; TASP
+// = the same AllGather split into one piece per Hamiltonian ring per
+// iteration). out[(t-1)*P*P + src*P + dst] += bytes. With needed_only, a
+// reception counts only if the receiver or a rank after it on the same ring
+// (within the iterations that remain) has a valid pair with the block.
+int oracle_link_bytes(int kind, int P, int T, const int32_t* cu, int ndocs, int causal,
+                      const int32_t* succ, long long bytes_per_token, int needed_only,
+                      long long* out) {
+  if (P < 2) return 0;
+  if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return 1;
+  if (kind == 1 && T % (2 * P) != 0) return 2;
+  const size_t PP = static_cast<size_t>(P) * P;
+  for (size_t i = 0; i < static_cast<size_t>(P - 1) * PP; ++i) out[i] = 0;
+  auto chunk = [&](int x, int* a, int* b) { split_bounds(T, P, x, a, b); };
+  // Q ranges of rank r.
+  auto qranges = [&](int r, std::vector<std::pair<int, int>>& q) {
+    q.clear();
+    if (kind == 1) {
+      const int c = T / (2 * P);
+      q.push_back({r * c, (r + 1) * c});
+      q.push_back({(2 * P - 1 - r) * c, (2 * P - r) * c});
+    } else {
+      int a, b;
+      chunk(r, &a, &b);
+      q.push_back({a, b});
+    }
+  };
+  auto wants = [&](int r, int ka, int kb) {
+    std::vector<std::pair<int, int>> q;
+    qranges(r, q);
+    for (auto& x : q)
+      if (oracle_valid_pairs(cu, ndocs, causal, x.first, x.second, ka, kb) > 0) return true;
+    return false;
+  };
+  for (int t = 1; t < P; ++t) {
+    for (int r = 0; r < P; ++r) {
+      if (kind == 0 || kind == 1) {
+        const int src_rank = ((r - t) % P + P) % P;  // whose chunk(s) arrive
+        const int from = (r + P - 1) % P;
+        std::vector<std::pair<int, int>> blocks;
+        if (kind == 0) {
+          int a, b;
+          chunk(src_rank, &a, &b);
+          blocks.push_back({a, b});
+        } else {
+          qranges(src_rank, blocks);
+        }
+        for (auto& bl : blocks) {
+          bool keep = !needed_only;
+          for (int k = 0; !keep && t + k <= P - 1; ++k)
+            if (wants((r + k) % P, bl.first, bl.second)) keep = true;
+          if (keep)
+            out[static_cast<size_t>(t - 1) * PP + static_cast<size_t>(from) * P + r] +=
+                (bl.second - bl.first) * bytes_per_token;
+        }
+      } else {
+        for (int c = 0; c < P - 1; ++c) {
+          const int32_t* sc = succ + static_cast<size_t>(c) * P;
+          // predecessor of r on ring c, and the rank t hops upstream
+          int from = -1;
+          for (int u = 0; u < P; ++u)
+            if (sc[u] == r) from = u;
+          int src_rank = r;
+          for (int h = 0; h < t; ++h)
+            for (int u = 0; u < P; ++u)
+              if (sc[u] == src_rank) { src_rank = u; break; }
+          int cb, ce, pb, pe;
+          chunk(src_rank, &cb, &ce);
+          split_bounds(ce - cb, P - 1, c, &pb, &pe);
+          const int ka = cb + pb, kb = cb + pe;
+          if (kb <= ka) continue;
+          bool keep = !needed_only;
+          int v = r;
+          for (int k = 0; !keep && t + k <= P - 1; ++k) {
+            if (wants(v, ka, kb)) keep = true;
+            v = sc[v];
+          }
+          if (keep)
+            out[static_cast<size_t>(t - 1) * PP + static_cast<size_t>(from) * P + r] +=
+                (kb - ka) * bytes_per_token;
+        }
+      }
+    }
+  }
+  return 0;
+}
+
 }  // extern "C"

@@ -25,7 +25,7 @@ SP_DTYPE_BF16, SP_DTYPE_FP32 = 0, 1
 _STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_ERR_BUFFER_TOO_SMALL",
            4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_INTERNAL"}
 
-EXPORTED = ["sp_schedule_build", "sp_tasp_cycles", "sp_partial_attn", "sp_lse_merge",
+EXPORTED = ["sp_schedule_build", "sp_tasp_cycles", "sp_schedule_link_bytes", "sp_partial_attn", "sp_lse_merge",
             "sp_packed_attention_workspace_size", "sp_packed_attention",
             "sp_packed_attention_static_ws", "sp_check_device_status",
             "sp_selftest_bounded_wait", "sp_status_string"]
@@ -60,6 +60,8 @@ def load():
                                           ctypes.POINTER(i64)]
         lib.sp_tasp_cycles.restype = ctypes.c_int
         lib.sp_tasp_cycles.argtypes = [i32, u64, vp]
+        lib.sp_schedule_link_bytes.restype = ctypes.c_int
+        lib.sp_schedule_link_bytes.argtypes = [ctypes.c_int, i32, i32, vp, i32, i32, u64, i64, i32, vp]
         lib.sp_partial_attn.restype = ctypes.c_int
         lib.sp_partial_attn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int,
                                         i32, i32, i32, i32, vp, i32, i32, f32, vp]
@@ -114,6 +116,20 @@ def sp_tasp_cycles(P: int, seed: int = 0) -> np.ndarray:
     lib = load()
     out = np.zeros((max(P - 1, 0), P), dtype=np.int32)
     _check(lib.sp_tasp_cycles(P, seed, out.ctypes.data if out.size else None), "sp_tasp_cycles")
+    return out
+
+
+def sp_schedule_link_bytes(kind: int, P: int, total_tokens: int, cu_seqlens, causal: bool,
+                           seed: int = 0, bytes_per_token: int = 1,
+                           needed_only: bool = False) -> np.ndarray:
+    """Bytes per directed link per transfer iteration: int64 [P-1, P, P] (src, dst)."""
+    lib = load()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    out = np.zeros((max(P - 1, 0), P, P), dtype=np.int64)
+    _check(lib.sp_schedule_link_bytes(kind, P, total_tokens, cu.ctypes.data, len(cu) - 1, int(causal),
+                                      seed, bytes_per_token, int(needed_only),
+                                      out.ctypes.data if out.size else None),
+           "sp_schedule_link_bytes")
     return out
 
 

@@ -399,3 +399,84 @@ sp_status sp_schedule_build(sp_sched_kind kind, int32_t P, int32_t T, const int3
 }
 
 }  // extern "C"
+
+extern "C" sp_status sp_schedule_link_bytes(sp_sched_kind kind, int32_t P, int32_t T,
+                                            const int32_t* cu, int32_t ndocs, int32_t causal_i,
+                                            uint64_t seed, int64_t bytes_per_token,
+                                            int32_t needed_only, int64_t* out) {
+  if (P < 1 || T < 1 || bytes_per_token < 0 || (P > 1 && !out)) return SP_ERR_INVALID_ARG;
+  if (kind != SP_SCHED_RING && kind != SP_SCHED_ZIGZAG && kind != SP_SCHED_TASP)
+    return SP_ERR_INVALID_ARG;
+  if (!valid_cu(cu, ndocs, T)) return SP_ERR_INVALID_ARG;
+  if (kind == SP_SCHED_ZIGZAG && (T % (2 * P)) != 0) return SP_ERR_UNSUPPORTED;
+  if (kind == SP_SCHED_TASP && (P == 4 || P == 6 || P > 64)) return SP_ERR_UNSUPPORTED;
+  if (P == 1) return SP_OK;  // nothing moves
+  const bool causal = causal_i != 0;
+  Docs docs{cu, ndocs};
+  const size_t PP = static_cast<size_t>(P) * P;
+  for (size_t i = 0; i < static_cast<size_t>(P - 1) * PP; ++i) out[i] = 0;
+
+  // Q ranges of each rank.
+  std::vector<std::vector<std::pair<int, int>>> own(P);
+  for (int r = 0; r < P; ++r) {
+    if (kind == SP_SCHED_ZIGZAG) {
+      const int c = T / (2 * P);
+      own[r].push_back({r * c, (r + 1) * c});
+      own[r].push_back({(2 * P - 1 - r) * c, (2 * P - r) * c});
+    } else {
+      int a, b;
+      split_bounds(T, P, r, &a, &b);
+      own[r].push_back({a, b});
+    }
+  }
+  auto needs = [&](int r, int ka, int kb) {
+    for (const auto& q : own[r])
+      if (docs.any_valid(q.first, q.second, ka, kb, causal)) return true;
+    return false;
+  };
+  // One block of keys [ka, kb) travelling along a ring whose successor is
+  // next(): it starts at rank `origin` and reaches the rank h hops downstream
+  // in iteration h (h = 1 .. P-1).
+  auto route = [&](int origin, int ka, int kb, auto&& next) {
+    if (kb <= ka) return;
+    std::vector<int> path(P);
+    path[0] = origin;
+    for (int h = 1; h < P; ++h) path[h] = next(path[h - 1]);
+    // last hop whose receiver (or someone after it) still needs the block
+    int last = P - 1;
+    if (needed_only) {
+      last = 0;
+      for (int h = P - 1; h >= 1; --h)
+        if (needs(path[h], ka, kb)) { last = h; break; }
+    }
+    const int64_t bytes = static_cast<int64_t>(kb - ka) * bytes_per_token;
+    for (int h = 1; h <= last; ++h)
+      out[static_cast<size_t>(h - 1) * PP + static_cast<size_t>(path[h - 1]) * P + path[h]] += bytes;
+  };
+
+  if (kind == SP_SCHED_RING || kind == SP_SCHED_ZIGZAG) {
+    auto next = [&](int r) { return (r + 1) % P; };
+    for (int x = 0; x < P; ++x) {
+      if (kind == SP_SCHED_RING) {
+        int a, b;
+        split_bounds(T, P, x, &a, &b);
+        route(x, a, b, next);
+      } else {
+        for (const auto& q : own[x]) route(x, q.first, q.second, next);
+      }
+    }
+    return SP_OK;
+  }
+  std::vector<int> succ;
+  if (!cached_decomposition(P, seed, succ)) return SP_ERR_INTERNAL;
+  for (int c = 0; c < P - 1; ++c) {
+    auto next = [&](int r) { return succ[static_cast<size_t>(c) * P + r]; };
+    for (int x = 0; x < P; ++x) {
+      int cb, ce, pb, pe;
+      split_bounds(T, P, x, &cb, &ce);
+      split_bounds(ce - cb, P - 1, c, &pb, &pe);
+      route(x, cb + pb, cb + pe, next);
+    }
+  }
+  return SP_OK;
+}
