@@ -48,6 +48,11 @@ def _load():
                                     ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_double, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
                                     ctypes.c_int, f64p, f64p, ctypes.c_int]
+        lib.oracle_attn_backward.restype = ctypes.c_int
+        lib.oracle_attn_backward.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_double, f64p, f64p, f64p,
+                                             ctypes.c_int]
         lib.oracle_lse_merge.restype = None
         lib.oracle_lse_merge.argtypes = [f64p, f64p, f64p, f64p, ctypes.c_longlong, ctypes.c_int,
                                          f64p, f64p]
@@ -136,6 +141,33 @@ def attn(q, k, v, cu_seqlens, causal: bool, scale: float | None = None, rows=Non
     if rc != 0:
         raise ValueError(f"oracle_attn rejected its arguments (code {rc})")
     return o, lse
+
+
+def attn_backward(q, k, v, dout, cu_seqlens, causal: bool, scale: float | None = None,
+                  threads: int = 0):
+    """Gradients (dq [T,Hq,d], dk [T,Hkv,d], dv [T,Hkv,d]) in fp64 of the masked
+    attention for the output gradient dout [T,Hq,d]."""
+    lib = _load()
+    q, dt = _as_input(q)
+    k, dk_ = _as_input(k)
+    v, dv_ = _as_input(v)
+    dout, dd = _as_input(dout)
+    assert dt == dk_ == dv_ == dd
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    cu, cup = _i32(cu_seqlens)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.empty((T, Hq, d))
+    dk = np.empty((T, Hkv, d))
+    dv = np.empty((T, Hkv, d))
+    f = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    rc = lib.oracle_attn_backward(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, dt,
+                                  T, Hq, Hkv, d, cup, len(cu) - 1, int(causal), float(scale),
+                                  f(dq), f(dk), f(dv), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_backward rejected its arguments (code {rc})")
+    return dq, dk, dv
 
 
 def lse_merge(o1, l1, o2, l2):

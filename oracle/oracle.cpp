@@ -418,6 +418,81 @@ int oracle_check_schedule(int kind, int P, int T, const int32_t* cu, int ndocs, 
   return 0;
 }
 
+// Gradients of the masked attention (the backward of the operation above):
+// with P_ij = exp(s_ij - LSE_i) over the valid keys j of query i,
+//   dV_j  = sum_i P_ij dO_i,              dP_ij = dO_i . v_j,
+//   D_i   = sum_j P_ij dP_ij (= dO_i . O_i),  dS_ij = P_ij (dP_ij - D_i),
+//   dQ_i  = scale sum_j dS_ij k_j,        dK_j  = scale sum_i dS_ij q_i,
+// where dK and dV of key/value head g sum over the query heads h with
+// h / (Hq/Hkv) == g. LSE and O are recomputed here in fp64 from q, k, v.
+// Layouts as oracle_attn; dq_out [T][Hq][d], dk_out / dv_out [T][Hkv][d].
+int oracle_attn_backward(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                         int T, int Hq, int Hkv, int d, const int32_t* cu, int ndocs, int causal,
+                         double scale, double* dq_out, double* dk_out, double* dv_out,
+                         int nthreads) {
+  if (T <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return 1;
+  if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return 2;
+  const int G = Hq / Hkv;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  for (size_t x = 0; x < static_cast<size_t>(T) * Hq * d; ++x) dq_out[x] = 0.0;
+  for (size_t x = 0; x < static_cast<size_t>(T) * Hkv * d; ++x) dk_out[x] = dv_out[x] = 0.0;
+  // One key/value head per task, so dK and dV of that head have one writer.
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int g = 0; g < Hkv; ++g) {
+    std::vector<double> qi(d), doi(d), s, p, o(d);
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      for (int i = 0; i < T; ++i) {
+        const int D = doc_of(cu, ndocs, i);
+        const int j0 = cu[D];
+        const int j1 = causal ? std::min(cu[D + 1], i + 1) : cu[D + 1];
+        const size_t qb = (static_cast<size_t>(i) * Hq + h) * d;
+        for (int c = 0; c < d; ++c) {
+          qi[c] = widen(q, dtype, qb + c);
+          doi[c] = widen(dout, dtype, qb + c);
+        }
+        s.resize(j1 - j0);
+        p.resize(j1 - j0);
+        double m = NEG_INF;
+        for (int j = j0; j < j1; ++j) {
+          const size_t kb = (static_cast<size_t>(j) * Hkv + g) * d;
+          double dot = 0.0;
+          for (int c = 0; c < d; ++c) dot += qi[c] * widen(k, dtype, kb + c);
+          s[j - j0] = dot * scale;
+          m = std::max(m, s[j - j0]);
+        }
+        double sum = 0.0;
+        for (int j = j0; j < j1; ++j) sum += std::exp(s[j - j0] - m);
+        const double lse = m + std::log(sum);
+        std::fill(o.begin(), o.end(), 0.0);
+        for (int j = j0; j < j1; ++j) {
+          p[j - j0] = std::exp(s[j - j0] - lse);
+          const size_t vb = (static_cast<size_t>(j) * Hkv + g) * d;
+          for (int c = 0; c < d; ++c) o[c] += p[j - j0] * widen(v, dtype, vb + c);
+        }
+        double Di = 0.0;
+        for (int c = 0; c < d; ++c) Di += doi[c] * o[c];
+        for (int j = j0; j < j1; ++j) {
+          const size_t kb = (static_cast<size_t>(j) * Hkv + g) * d;
+          double dp = 0.0;
+          for (int c = 0; c < d; ++c) dp += doi[c] * widen(v, dtype, kb + c);
+          const double pij = p[j - j0];
+          const double ds = pij * (dp - Di);
+          for (int c = 0; c < d; ++c) {
+            dv_out[kb + c] += pij * doi[c];
+            dq_out[qb + c] += scale * ds * widen(k, dtype, kb + c);
+            dk_out[kb + c] += scale * ds * qi[c];
+          }
+        }
+      }
+    }
+  }
+  return 0;
+}
+
 // Communication model of a schedule, stated from the receiving side: in
 // iteration t (1..P-1) of the AllGather, what does each rank receive and from
 // whom (TASP abstract: Ring AllGather = P-1 iterations of ring transfers; TASP
