@@ -15,7 +15,7 @@ LIB = os.path.join(HERE, "libsp_attn.so")
 
 CU_SOURCES = ["sp_api.cu", "attn_tc.cu", "attn_simt.cu", "sp_aux.cu"]
 CPP_SOURCES = ["sp_schedule.cpp"]
-HEADERS = ["sp_internal.h", "sp_device.cuh", "sp_workspace.h"]
+HEADERS = ["sp_internal.h", "sp_device.cuh", "sp_workspace.h", "sp_tiles.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
