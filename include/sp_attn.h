@@ -212,6 +212,39 @@ sp_status sp_packed_attention_static_ws(const void* q, const void* k, const void
                                         float scale, const sp_item* items_dev, int64_t n_items,
                                         void* stream);
 
+/* Bytes of device workspace sp_packed_attention_backward needs. */
+size_t sp_packed_attention_backward_workspace_size(int64_t n_items, int32_t T, int32_t Hq);
+
+/* sp_packed_attention_backward — gradients of sp_packed_attention for
+ * training with the sequence-parallel schedules (HSAP abstract: training
+ * throughput in tokens per GPU per second). With P_tj = exp(scale q_t.k_j -
+ * LSE_t) over the keys the mask allows, D_t = dO_t . O_t, dP_tj = dO_t . v_j,
+ * dS_tj = P_tj (dP_tj - D_t):
+ *   dQ_t = scale sum_j dS_tj k_j,  dK_j = scale sum_t dS_tj q_t,
+ *   dV_j = sum_t P_tj dO_t,
+ * dK and dV of a key/value head summing over the query heads of its group.
+ *  q, k, v, o, dout: device bf16 as in sp_packed_attention (o and lse are the
+ *     forward's outputs for the same inputs; dout has the layout of o).
+ *  lse: device float32 [Hq][T], natural log, as the forward wrote it.
+ *  dq: device bf16 [T][Hq][d]; dk, dv: device bf16 [T][Hkv][d]; every element
+ *     is written (keys no query attends get 0).
+ *  items_dev: a complete schedule (every pair the mask allows exactly once,
+ *     as sp_schedule_build produces). dQ walks the items like the forward;
+ *     dK and dV are accumulated key-tile by key-tile over the pairs the mask
+ *     allows, which for a complete schedule is the same set.
+ *  dtype must be SP_DTYPE_BF16 (SP_ERR_UNSUPPORTED otherwise); d is 64 or 128.
+ *  workspace: device, at least sp_packed_attention_backward_workspace_size
+ *     bytes, owned by the caller; calls sharing it must not overlap in time.
+ *  Timeouts of the kernels' bounded waits are reported through
+ *  sp_check_device_status. */
+sp_status sp_packed_attention_backward(const void* q, const void* k, const void* v, const void* o,
+                                       const void* dout, const float* lse, void* dq, void* dk,
+                                       void* dv, int32_t T, int32_t Hq, int32_t Hkv, int32_t d,
+                                       sp_dtype dtype, const int32_t* cu_seqlens_dev, int32_t ndocs,
+                                       int32_t causal, float scale, const sp_item* items_dev,
+                                       int64_t n_items, void* workspace, size_t workspace_bytes,
+                                       void* stream);
+
 /* Synchronises `stream`, reads and clears the current device's error word, and
  * returns SP_OK, SP_ERR_TIMEOUT, SP_ERR_INTERNAL, or SP_ERR_CUDA when the
  * stream itself reports a CUDA error. */

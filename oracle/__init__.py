@@ -53,6 +53,12 @@ def _load():
                                              ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_double, f64p, f64p, f64p,
                                              ctypes.c_int]
+        lib.oracle_attn_backward_sampled.restype = ctypes.c_int
+        lib.oracle_attn_backward_sampled.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_double, i32p,
+                                                     ctypes.c_int, f64p, i32p, ctypes.c_int, f64p, f64p,
+                                                     ctypes.c_int]
         lib.oracle_lse_merge.restype = None
         lib.oracle_lse_merge.argtypes = [f64p, f64p, f64p, f64p, ctypes.c_longlong, ctypes.c_int,
                                          f64p, f64p]
@@ -167,6 +173,35 @@ def attn_backward(q, k, v, dout, cu_seqlens, causal: bool, scale: float | None =
                                   f(dq), f(dk), f(dv), int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attn_backward rejected its arguments (code {rc})")
+    return dq, dk, dv
+
+
+def attn_backward_sampled(q, k, v, dout, cu_seqlens, causal: bool, qrows=(), krows=(),
+                          scale: float | None = None, threads: int = 0):
+    """fp64 gradients at chosen outputs: dq of the rows qrows [nq, Hq, d], and
+    dk, dv of the keys krows [nk, Hkv, d]. Same definitions as attn_backward."""
+    lib = _load()
+    q, dt = _as_input(q)
+    k, dk_ = _as_input(k)
+    v, dv_ = _as_input(v)
+    dout, dd = _as_input(dout)
+    assert dt == dk_ == dv_ == dd
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    cu, cup = _i32(cu_seqlens)
+    qr, qrp = _i32(np.asarray(qrows, dtype=np.int64).reshape(-1))
+    kr, krp = _i32(np.asarray(krows, dtype=np.int64).reshape(-1))
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.empty((len(qr), Hq, d))
+    dk = np.empty((len(kr), Hkv, d))
+    dv = np.empty((len(kr), Hkv, d))
+    f = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    rc = lib.oracle_attn_backward_sampled(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+                                          dt, T, Hq, Hkv, d, cup, len(cu) - 1, int(causal), float(scale),
+                                          qrp, len(qr), f(dq), krp, len(kr), f(dk), f(dv), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_backward_sampled rejected its arguments (code {rc})")
     return dq, dk, dv
 
 

@@ -493,6 +493,148 @@ int oracle_attn_backward(const void* q, const void* k, const void* v, const void
   return 0;
 }
 
+// The same gradients restricted to chosen outputs, for checking a large
+// problem on samples: dQ of the listed query rows, and dK, dV of the listed
+// keys. Each value follows the definitions above term by term; a query's LSE
+// and D are recomputed from q, k, v over its own valid keys (once per query
+// and head, since several keys share the queries that attend them).
+//  qrows[nq] -> dq_rows [nq][Hq][d];  krows[nk] -> dk_rows, dv_rows [nk][Hkv][d].
+namespace {
+
+struct RowStats {
+  double lse, D;
+};
+
+// LSE and D = dO . O of query i under head h (g = its key/value head).
+RowStats row_stats(const void* q, const void* k, const void* v, const void* dout, int dtype, int Hq,
+                   int Hkv, int d, const int32_t* cu, int ndocs, int causal, double scale, int i,
+                   int h, int g) {
+  const int D = doc_of(cu, ndocs, i);
+  const int j0 = cu[D];
+  const int j1 = causal ? std::min(cu[D + 1], i + 1) : cu[D + 1];
+  const size_t qb = (static_cast<size_t>(i) * Hq + h) * d;
+  std::vector<double> s(j1 - j0), o(d, 0.0);
+  double m = NEG_INF;
+  for (int j = j0; j < j1; ++j) {
+    const size_t kb = (static_cast<size_t>(j) * Hkv + g) * d;
+    double dot = 0.0;
+    for (int c = 0; c < d; ++c) dot += widen(q, dtype, qb + c) * widen(k, dtype, kb + c);
+    s[j - j0] = dot * scale;
+    m = std::max(m, s[j - j0]);
+  }
+  double sum = 0.0;
+  for (int j = j0; j < j1; ++j) sum += std::exp(s[j - j0] - m);
+  RowStats r;
+  r.lse = m + std::log(sum);
+  for (int j = j0; j < j1; ++j) {
+    const double pij = std::exp(s[j - j0] - r.lse);
+    const size_t vb = (static_cast<size_t>(j) * Hkv + g) * d;
+    for (int c = 0; c < d; ++c) o[c] += pij * widen(v, dtype, vb + c);
+  }
+  r.D = 0.0;
+  for (int c = 0; c < d; ++c) r.D += widen(dout, dtype, qb + c) * o[c];
+  return r;
+}
+
+// P_ij, dP_ij for query i (head h) and key j (key/value head g).
+void pair_terms(const void* q, const void* k, const void* v, const void* dout, int dtype, int Hq,
+                int Hkv, int d, double scale, int i, int h, int j, int g, const RowStats& st,
+                double* p, double* dp) {
+  const size_t qb = (static_cast<size_t>(i) * Hq + h) * d;
+  const size_t kb = (static_cast<size_t>(j) * Hkv + g) * d;
+  double dot = 0.0, dpd = 0.0;
+  for (int c = 0; c < d; ++c) {
+    dot += widen(q, dtype, qb + c) * widen(k, dtype, kb + c);
+    dpd += widen(dout, dtype, qb + c) * widen(v, dtype, kb + c);
+  }
+  *p = std::exp(dot * scale - st.lse);
+  *dp = dpd;
+}
+
+}  // namespace
+
+int oracle_attn_backward_sampled(const void* q, const void* k, const void* v, const void* dout,
+                                 int dtype, int T, int Hq, int Hkv, int d, const int32_t* cu,
+                                 int ndocs, int causal, double scale, const int32_t* qrows, int nq,
+                                 double* dq_rows, const int32_t* krows, int nk, double* dk_rows,
+                                 double* dv_rows, int nthreads) {
+  if (T <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || nq < 0 || nk < 0) return 1;
+  if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return 2;
+  for (int x = 0; x < nq; ++x)
+    if (qrows[x] < 0 || qrows[x] >= T) return 3;
+  for (int x = 0; x < nk; ++x)
+    if (krows[x] < 0 || krows[x] >= T) return 3;
+  const int G = Hq / Hkv;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  // dQ_i = scale sum_j dS_ij k_j over the valid keys of row i.
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (int x = 0; x < nq; ++x)
+    for (int h = 0; h < Hq; ++h) {
+      const int i = qrows[x], g = h / G;
+      const RowStats st = row_stats(q, k, v, dout, dtype, Hq, Hkv, d, cu, ndocs, causal, scale, i, h, g);
+      const int D = doc_of(cu, ndocs, i);
+      const int j1 = causal ? std::min(cu[D + 1], i + 1) : cu[D + 1];
+      double* out = dq_rows + (static_cast<size_t>(x) * Hq + h) * d;
+      for (int c = 0; c < d; ++c) out[c] = 0.0;
+      for (int j = cu[D]; j < j1; ++j) {
+        double p, dp;
+        pair_terms(q, k, v, dout, dtype, Hq, Hkv, d, scale, i, h, j, g, st, &p, &dp);
+        const double ds = p * (dp - st.D);
+        const size_t kb = (static_cast<size_t>(j) * Hkv + g) * d;
+        for (int c = 0; c < d; ++c) out[c] += scale * ds * widen(k, dtype, kb + c);
+      }
+    }
+  if (nk == 0) return 0;
+  // The queries that attend some listed key, and their statistics per head.
+  std::vector<int> need;
+  {
+    std::vector<char> mark(T, 0);
+    for (int x = 0; x < nk; ++x) {
+      const int j = krows[x];
+      const int D = doc_of(cu, ndocs, j);
+      for (int i = causal ? j : cu[D]; i < cu[D + 1]; ++i) mark[i] = 1;
+    }
+    for (int i = 0; i < T; ++i)
+      if (mark[i]) need.push_back(i);
+  }
+  std::vector<int> slot(T, -1);
+  for (size_t n = 0; n < need.size(); ++n) slot[need[n]] = static_cast<int>(n);
+  std::vector<RowStats> stats(need.size() * Hq);
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (long long n = 0; n < static_cast<long long>(need.size()); ++n)
+    for (int h = 0; h < Hq; ++h)
+      stats[n * Hq + h] = row_stats(q, k, v, dout, dtype, Hq, Hkv, d, cu, ndocs, causal, scale,
+                                    need[n], h, h / G);
+  // dV_j = sum_i P_ij dO_i and dK_j = scale sum_i dS_ij q_i over the queries
+  // attending j and the query heads of j's key/value head.
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (int x = 0; x < nk; ++x)
+    for (int g = 0; g < Hkv; ++g) {
+      const int j = krows[x];
+      const int D = doc_of(cu, ndocs, j);
+      double* dk = dk_rows + (static_cast<size_t>(x) * Hkv + g) * d;
+      double* dv = dv_rows + (static_cast<size_t>(x) * Hkv + g) * d;
+      for (int c = 0; c < d; ++c) dk[c] = dv[c] = 0.0;
+      for (int h = g * G; h < (g + 1) * G; ++h)
+        for (int i = causal ? j : cu[D]; i < cu[D + 1]; ++i) {
+          const RowStats& st = stats[static_cast<size_t>(slot[i]) * Hq + h];
+          double p, dp;
+          pair_terms(q, k, v, dout, dtype, Hq, Hkv, d, scale, i, h, j, g, st, &p, &dp);
+          const double ds = p * (dp - st.D);
+          const size_t qb = (static_cast<size_t>(i) * Hq + h) * d;
+          for (int c = 0; c < d; ++c) {
+            dv[c] += p * widen(dout, dtype, qb + c);
+            dk[c] += scale * ds * widen(q, dtype, qb + c);
+          }
+        }
+    }
+  return 0;
+}
+
 // Communication model of a schedule, stated from the receiving side: in
 // iteration t (1..P-1) of the AllGather, what does each rank receive and from
 // whom (TASP abstract: Ring AllGather = P-1 iterations of ring transfers; TASP

@@ -27,7 +27,8 @@ _STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_
 
 EXPORTED = ["sp_schedule_build", "sp_tasp_cycles", "sp_schedule_link_bytes", "sp_partial_attn", "sp_lse_merge",
             "sp_packed_attention_workspace_size", "sp_packed_attention",
-            "sp_packed_attention_static_ws", "sp_check_device_status",
+            "sp_packed_attention_static_ws", "sp_packed_attention_backward_workspace_size",
+            "sp_packed_attention_backward", "sp_check_device_status",
             "sp_selftest_bounded_wait", "sp_status_string"]
 
 
@@ -75,6 +76,12 @@ def load():
         lib.sp_packed_attention_static_ws.restype = ctypes.c_int
         lib.sp_packed_attention_static_ws.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                       ctypes.c_int, vp, i32, i32, f32, vp, i64, vp]
+        lib.sp_packed_attention_backward_workspace_size.restype = ctypes.c_size_t
+        lib.sp_packed_attention_backward_workspace_size.argtypes = [i64, i32, i32]
+        lib.sp_packed_attention_backward.restype = ctypes.c_int
+        lib.sp_packed_attention_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                     i32, ctypes.c_int, vp, i32, i32, f32, vp, i64,
+                                                     vp, ctypes.c_size_t, vp]
         lib.sp_check_device_status.restype = ctypes.c_int
         lib.sp_check_device_status.argtypes = [vp]
         lib.sp_selftest_bounded_wait.restype = ctypes.c_int
@@ -251,6 +258,34 @@ def sp_packed_attention_static_ws(q, k, v, o, lse, cu_seqlens, causal: bool, ite
                                                 _stream(stream)), "sp_packed_attention_static_ws")
 
 
+def sp_packed_attention_backward_workspace_size(n_items: int, T: int, Hq: int) -> int:
+    return int(load().sp_packed_attention_backward_workspace_size(int(n_items), int(T), int(Hq)))
+
+
+def sp_packed_attention_backward(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, causal: bool,
+                                 items_dev, workspace, scale: float | None = None, stream=None):
+    """Gradients of sp_packed_attention (bf16): dq [T, Hq, d], dk and dv [T, Hkv, d];
+    o, lse: the forward's outputs; dout: the gradient of o; workspace: uint8 device
+    tensor of sp_packed_attention_backward_workspace_size(n, T, Hq) bytes."""
+    T, Hq, Hkv, d = _check_qkv(q, k, v)
+    torch = _torch()
+    for name, t, shape in (("o", o, (T, Hq, d)), ("dout", dout, (T, Hq, d)), ("dq", dq, (T, Hq, d)),
+                           ("dk", dk, (T, Hkv, d)), ("dv", dv, (T, Hkv, d))):
+        _need(t.dtype == q.dtype and tuple(t.shape) == shape and t.is_contiguous() and t.is_cuda,
+              f"{name} must be contiguous {q.dtype} {list(shape)} on device")
+    _need(lse.dtype == torch.float32 and tuple(lse.shape) == (Hq, T) and lse.is_contiguous(),
+          "lse must be fp32 [Hq, T]")
+    _need(items_dev.dtype == torch.int32 and items_dev.is_cuda and items_dev.dim() == 2 and
+          items_dev.shape[1] == 8 and items_dev.is_contiguous(), "items_dev: int32 [n, 8] on device")
+    _need(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_cuda, "cu_seqlens must be int32 on device")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    _check(load().sp_packed_attention_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), T, Hq,
+        Hkv, d, _dtype_code(q), _ptr(cu_seqlens), cu_seqlens.numel() - 1, int(causal), scale,
+        _ptr(items_dev), items_dev.shape[0], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "sp_packed_attention_backward")
+
+
 def sp_check_device_status(stream=None):
     _check(load().sp_check_device_status(_stream(stream)), "device status")
 
@@ -290,3 +325,17 @@ class PackedAttention:
         sp_packed_attention(q, k, v, o, lse, self.cu_dev, self.causal, self.items_dev, self.workspace,
                             scale=scale, stream=stream)
         return o, lse
+
+    def backward(self, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale=None, stream=None):
+        """Gradients (dq, dk, dv) of the forward call that returned (o, lse)."""
+        torch = _torch()
+        T, Hq, d = q.shape
+        nbytes = sp_packed_attention_backward_workspace_size(len(self.items), T, Hq)
+        if getattr(self, "bwd_workspace", None) is None or self.bwd_workspace.numel() < nbytes:
+            self.bwd_workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        sp_packed_attention_backward(q, k, v, o, dout, lse, dq, dk, dv, self.cu_dev, self.causal,
+                                     self.items_dev, self.bwd_workspace, scale=scale, stream=stream)
+        return dq, dk, dv

@@ -232,6 +232,71 @@ sp_status sp_packed_attention(const void* q, const void* k, const void* v, void*
   return launch_attention(a, dtype, sms, st, 0);
 }
 
+size_t sp_packed_attention_backward_workspace_size(int64_t n_items, int32_t T, int32_t Hq) {
+  if (n_items < 0) n_items = 0;
+  if (T < 0) T = 0;
+  if (Hq < 0) Hq = 0;
+  const size_t rowdot = (static_cast<size_t>(T) * Hq * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  return sp::ws_layout(n_items).total + rowdot;
+}
+
+sp_status sp_packed_attention_backward(const void* q, const void* k, const void* v, const void* o,
+                                       const void* dout, const float* lse, void* dq, void* dk,
+                                       void* dv, int32_t T, int32_t Hq, int32_t Hkv, int32_t d,
+                                       sp_dtype dtype, const int32_t* cu_seqlens_dev, int32_t ndocs,
+                                       int32_t causal, float scale, const sp_item* items_dev,
+                                       int64_t n_items, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  sp_status s = check_shapes(T, Hq, Hkv, d, dtype, ndocs, scale);
+  if (s != SP_OK) return s;
+  if (dtype != SP_DTYPE_BF16) return SP_ERR_UNSUPPORTED;
+  if (n_items < 0 || n_items > 0x7fffffffll) return SP_ERR_INVALID_ARG;
+  if (T == 0) return SP_OK;
+  if (n_items == 0) return SP_ERR_INVALID_ARG;  // a complete schedule has items whenever T > 0
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !cu_seqlens_dev || !items_dev ||
+      !workspace)
+    return SP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(items_dev) ||
+      !aligned16(workspace))
+    return SP_ERR_INVALID_ARG;
+  if (workspace_bytes < sp_packed_attention_backward_workspace_size(n_items, T, Hq))
+    return SP_ERR_BUFFER_TOO_SMALL;
+  unsigned* err;
+  int sms;
+  if (!device_state(&err, &sms)) return SP_ERR_CUDA;
+  if (!encoder()) return SP_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const sp::WsLayout L = sp::ws_layout(n_items);
+  float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.total);
+
+  const long long warps = static_cast<long long>(T) * Hq;
+  long long g = (warps + 7) / 8;
+  if (g > static_cast<long long>(sms) * 16) g = static_cast<long long>(sms) * 16;
+  cudaError_t e = sp::launch_bwd_rowdot(o, dout, dvec, T, Hq, d, static_cast<int>(g), st);
+  if (e != cudaSuccess) return SP_ERR_CUDA;
+  e = sp::launch_prep(items_dev, n_items, T, Hq, sp::BWD_ROWS_PER_UNIT, workspace, err, st);
+  if (e != cudaSuccess) return SP_ERR_CUDA;
+
+  sp::BwdArgs b;
+  std::memset(&b, 0, sizeof b);
+  b.fwd = base_args(q, k, v, nullptr, nullptr, T, Hq, Hkv, d, cu_seqlens_dev, ndocs, causal, scale, err);
+  b.fwd.items = items_dev;
+  b.fwd.header = static_cast<const int32_t*>(workspace);
+  b.fwd.segs = reinterpret_cast<const sp::SegEntry*>(static_cast<const char*>(workspace) + L.off_segs);
+  b.fwd.rows_per_unit = sp::BWD_ROWS_PER_UNIT;
+  b.lse = lse;
+  b.dvec = dvec;
+  b.dq = dq;
+  b.dk = dk;
+  b.dv = dv;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_map(&mq, q, T, Hq, d) || !encode_map(&mk, k, T, Hkv, d) || !encode_map(&mv, v, T, Hkv, d) ||
+      !encode_map(&mdo, dout, T, Hq, d))
+    return SP_ERR_CUDA;
+  return cuda_fail(sp::launch_bwd_tc(b, &mq, &mk, &mv, &mdo, sms, st));
+}
+
 sp_status sp_check_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return SP_ERR_CUDA;

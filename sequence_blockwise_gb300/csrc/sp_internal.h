@@ -58,6 +58,17 @@ struct AttnArgs {
   unsigned long long timeout_ns;
 };
 
+// Arguments of the backward kernels. fwd holds the forward's inputs, shapes
+// and schedule tables (its o and lse fields are unused).
+struct BwdArgs {
+  AttnArgs fwd;
+  const float* lse;   // [Hq][T] natural-log LSE written by the forward
+  const float* dvec;  // [Hq][T] D_i = dO_i . O_i
+  void* dq;           // bf16 [T][Hq][d]
+  void* dk;           // bf16 [T][Hkv][d]
+  void* dv;           // bf16 [T][Hkv][d]
+};
+
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_prep(const sp_item* items, int64_t n_items, int32_t T, int32_t Hq,
                         int32_t rows_per_unit, void* workspace, unsigned* err, cudaStream_t st);
@@ -66,10 +77,16 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const void* tmap_q, const void* tm
                            const void* tmap_v, int grid, cudaStream_t st);
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
                              int32_t rows, int32_t Hq, int32_t d, int grid, cudaStream_t st);
+cudaError_t launch_bwd_rowdot(const void* o, const void* dout, float* dvec, int T, int Hq, int d,
+                              int grid, cudaStream_t st);
+// dQ kernel (walks the schedule in fwd) then the dK/dV kernel, both bf16.
+cudaError_t launch_bwd_tc(const BwdArgs& a, const void* tmap_q, const void* tmap_k,
+                          const void* tmap_v, const void* tmap_do, int grid, cudaStream_t st);
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t st);
 
 // Rows per work unit of each kernel.
 constexpr int TC_ROWS_PER_UNIT = 256;
 constexpr int SIMT_ROWS_PER_UNIT = 128;
+constexpr int BWD_ROWS_PER_UNIT = 128;
 
 }  // namespace sp

@@ -117,3 +117,31 @@ def test_schedule_argument_checks():
     assert cap.value == 10
     # Empty sequence.
     assert len(sb.sp_schedule_build(sb.SP_SCHED_RING, 4, 0, [0], True)) == 0
+
+
+def test_backward_argument_checks():
+    lib = sb.load()
+
+    def bwd(n_items=10, ws_bytes=None, **kw):
+        a = dict(T=512, Hq=4, Hkv=2, d=128, dtype=0, nd=1, causal=1, scale=0.1, items=FAKE,
+                 dq=FAKE, dout=FAKE)
+        a.update(kw)
+        ws = (sb.sp_packed_attention_backward_workspace_size(n_items, a["T"], a["Hq"])
+              if ws_bytes is None else ws_bytes)
+        return lib.sp_packed_attention_backward(FAKE, FAKE, FAKE, FAKE, a["dout"], FAKE, a["dq"], FAKE,
+                                                FAKE, a["T"], a["Hq"], a["Hkv"], a["d"], a["dtype"],
+                                                FAKE, a["nd"], a["causal"], a["scale"], a["items"],
+                                                n_items, FAKE, ws, None)
+
+    assert bwd(dtype=1) == 2                      # fp32 backward not offered
+    assert bwd(d=32) == 2
+    assert bwd(Hq=3) == 1
+    assert bwd(T=0) == 0
+    assert bwd(n_items=0) == 1                    # T > 0 needs a schedule
+    assert bwd(n_items=-3) == 1
+    assert bwd(ws_bytes=64) == 3
+    assert bwd(dout=None) == 1
+    assert bwd(dq=ctypes.c_void_p(0x100008)) == 1  # misaligned
+    assert bwd(items=None) == 1
+    base = sb.sp_packed_attention_workspace_size(10)
+    assert sb.sp_packed_attention_backward_workspace_size(10, 512, 4) >= base + 512 * 4 * 4

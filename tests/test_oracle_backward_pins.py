@@ -83,3 +83,26 @@ def test_dk_sums_to_zero_per_document_and_isolation():
         assert np.array_equal(dq2[:17], np.zeros_like(dq2[:17]))
         assert np.array_equal(dk2[:17], np.zeros_like(dk2[:17]))
         assert np.array_equal(dq2[17:], dq[17:]) and np.array_equal(dv2[17:], dv[17:])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_sampled_gradients_match_full(causal):
+    """The sampled form (chosen dQ rows, chosen dK/dV keys) equals the pinned
+    full gradients at those positions, bf16 inputs, GQA, several documents."""
+    rng = np.random.default_rng(5)
+    T, Hq, Hkv, d = 61, 6, 2, 16
+    cu = np.array([0, 1, 20, 21, 61], dtype=np.int32)
+    bits = lambda shape: (rng.standard_normal(shape).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    q, k, v, w = bits((T, Hq, d)), bits((T, Hkv, d)), bits((T, Hkv, d)), bits((T, Hq, d))
+    dq, dk, dv = oracle.attn_backward(q, k, v, w, cu, causal)
+    qrows = np.array([0, 1, 5, 19, 20, 21, 40, 60])
+    krows = np.array([0, 2, 19, 20, 22, 59, 60])
+    sq, sk, sv = oracle.attn_backward_sampled(q, k, v, w, cu, causal, qrows, krows)
+    assert np.allclose(sq, dq[qrows], rtol=1e-12, atol=1e-13)
+    assert np.allclose(sk, dk[krows], rtol=1e-12, atol=1e-13)
+    assert np.allclose(sv, dv[krows], rtol=1e-12, atol=1e-13)
+    # Empty selections are allowed; out-of-range rows are rejected.
+    e = oracle.attn_backward_sampled(q, k, v, w, cu, causal)
+    assert e[0].shape == (0, Hq, d) and e[1].shape == (0, Hkv, d)
+    with pytest.raises(ValueError):
+        oracle.attn_backward_sampled(q, k, v, w, cu, causal, qrows=[T])
