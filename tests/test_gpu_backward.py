@@ -284,6 +284,8 @@ def test_backward_workload_parity(w):
     qi = torch.from_numpy(qrows).cuda()
     ki = torch.from_numpy(krows).cuda()
     for name, got, ref in (("dq", dq[qi], rq), ("dk", dk[ki], rk), ("dv", dv[ki], rv)):
+        if ref.shape[0] == 0:
+            continue
         g = got.double().cpu().numpy()
         err = float(np.abs(g - ref).max())
         mx = float(np.abs(ref).max())
