@@ -62,12 +62,13 @@ def kernel_traffic():
     """DRAM bytes per launch of the attention kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "attn_tc_traffic.json")
-    src = os.path.join(ROOT, "sequence_blockwise_gb300", "csrc", "attn_tc.cu")
     try:
         with open(path) as f:
             rec = json.load(f)
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if rec.get("attn_tc_cu_sha256") == sha:
+        h = hashlib.sha256()
+        for src in rec["kernel_sources"]:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        if rec.get("kernel_sources_sha256") == h.hexdigest():
             return float(rec["traffic_bytes_per_launch"])
     except Exception:
         pass
@@ -280,7 +281,40 @@ def run_ours(args, world, rank, local):
     e2e_value = world * flop * args.steps / (e2e_ms * 1e-3) / 1e12
     sb.sp_check_device_status(stream)
 
+    # ---- backward of the same call (dQ, dK, dV), timed on its own after the
+    # forward's timed region; reported beside the headline, not in `value`.
+    bwd = None
+    if not args.no_backward:
+        dout = wl.random_normal((w.T, w.Hq, w.d), w.seed + 99, dev, "bf16")
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        att(q, k, v, o, lse, stream=stream)
+
+        def bstep():
+            att.backward(q, k, v, o, lse, dout, dq, dk, dv, stream=stream)
+
+        for _ in range(max(args.warmup, 3)):
+            bstep()
+        torch.cuda.synchronize(dev)
+        bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            bev[i][0].record(stream)
+            bstep()
+            bev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        sb.sp_check_device_status(stream)
+        bper = [a.elapsed_time(b) for a, b in bev]
+        b_ms = dist_max(sum(bper) / len(bper), world)
+        bflop = 2.5 * flop  # QK^T and dO V^T recomputed, dV, dK, dQ: 10 d per pair and head
+        bwd = {"ms_per_call": round(b_ms, 4), "tflops": round(bflop / (b_ms * 1e-3) / 1e12, 2),
+               "flop_per_call": bflop, "flop_convention": "10*d*Hq*valid_pairs (2.5x forward)",
+               "frac_of_peak": None, "launches_per_call": 4,
+               "kernels": "bwd_rowdot, prep_kernel, bwd_dq_kernel<128>, bwd_dkdv_kernel<128>"}
+        del dout, dq, dk, dv
+
     peaks = read_peaks()
+    if bwd is not None:
+        bwd["frac_of_peak"] = round(bwd["tflops"] / peaks["bf16_tflops"], 4)
     avg_launch_ms = sum(per) / len(per)
     achieved = flop / (avg_launch_ms * 1e-3) / 1e12
     traffic = kernel_traffic()
@@ -322,6 +356,7 @@ def run_ours(args, world, rank, local):
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
+            "backward": bwd,
         }
     return result, w, cu
 
@@ -339,19 +374,28 @@ def kernel_only(args, local):
     att = sb.PackedAttention(cu, w.causal, w.kind, w.P, w.Hq, seed=w.seed, device=dev)
     o = torch.empty_like(q)
     lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
-    for _ in range(args.warmup):
+    if args.pass_ == "backward":
         att(q, k, v, o, lse)
+        dout = wl.random_normal((w.T, w.Hq, w.d), w.seed + 99, dev, "bf16")
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        run = lambda: att.backward(q, k, v, o, lse, dout, dq, dk, dv)
+        mult = 2.5
+    else:
+        run = lambda: att(q, k, v, o, lse)
+        mult = 1.0
+    for _ in range(args.warmup):
+        run()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
-        att(q, k, v, o, lse)
+        run()
     e1.record()
     torch.cuda.synchronize(dev)
     sb.sp_check_device_status()
     ms = e0.elapsed_time(e1) / max(1, args.steps)
-    flop = 4.0 * w.d * w.Hq * valid_pairs(cu, w.causal)
-    print(json.dumps({"kernel_only": True, "workload": w.name, "ms_per_step": ms,
+    flop = mult * 4.0 * w.d * w.Hq * valid_pairs(cu, w.causal)
+    print(json.dumps({"kernel_only": True, "pass": args.pass_, "workload": w.name, "ms_per_step": ms,
                       "tflops": flop / (ms * 1e-3) / 1e12}), flush=True)
 
 
@@ -364,6 +408,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward measurement reported beside the headline")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+                    help="with --kernel-only: which pass to run")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only W warm-up + K device-resident steps (driver for ncu captures)")
     args = ap.parse_args()
