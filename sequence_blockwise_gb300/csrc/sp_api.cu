@@ -60,14 +60,14 @@ bool encoder() {
   return true;
 }
 
-// Rank-3 bf16 map over [T][H][d] with a {64, 1, 128} box and 128-byte swizzle:
-// one load brings 128 tokens x 64 dims of one head, laid out as the tensor core
-// reads a K-major (Q, K) or MN-major (V) operand.
-bool encode_map(CUtensorMap* m, const void* base, int T, int H, int d) {
+// Rank-3 bf16 map over [T][H][d] with a {64, 1, box_rows} box and 128-byte
+// swizzle: one load brings box_rows tokens x 64 dims of one head, laid out as
+// the tensor core reads a K-major (Q, K) or MN-major (V) operand.
+bool encode_map(CUtensorMap* m, const void* base, int T, int H, int d, int box_rows = 128) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -291,8 +291,8 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   b.dk = dk;
   b.dv = dv;
   CUtensorMap mq, mk, mv, mdo;
-  if (!encode_map(&mq, q, T, Hq, d) || !encode_map(&mk, k, T, Hkv, d) || !encode_map(&mv, v, T, Hkv, d) ||
-      !encode_map(&mdo, dout, T, Hq, d))
+  if (!encode_map(&mq, q, T, Hq, d, 64) || !encode_map(&mk, k, T, Hkv, d, 64) ||
+      !encode_map(&mv, v, T, Hkv, d, 64) || !encode_map(&mdo, dout, T, Hq, d, 64))
     return SP_ERR_CUDA;
   return cuda_fail(sp::launch_bwd_tc(b, &mq, &mk, &mv, &mdo, sms, st));
 }
