@@ -102,6 +102,46 @@ sp_status sp_schedule_build(sp_sched_kind kind, int32_t P, int32_t total_tokens,
                             const int32_t* cu_seqlens_host, int32_t ndocs, int32_t causal,
                             uint64_t seed, sp_item* out_items, int64_t* inout_n_items);
 
+/* Chunking policies for the P contiguous chunks of RING and TASP schedules. */
+typedef enum {
+  SP_CHUNK_EQUAL = 0,        /* equal token counts (the first T mod P get one more) */
+  SP_CHUNK_BALANCED = 1,     /* equal attention work per chunk */
+  SP_CHUNK_BALANCED_DOC = 2  /* balanced, then boundaries moved onto nearby document starts */
+} sp_chunking;
+
+/* sp_chunk_bounds — host only; chunk boundaries out_bounds[0..P] (out_bounds[0]
+ * = 0, out_bounds[P] = T, non-decreasing) for the virtual ranks. Equal token
+ * counts leave a causal or packed sequence's attention work unevenly spread
+ * over the ranks (load balancing: "HSAP: A Hierarchical Sequence-aware
+ * Parallelism for Hybrid-Context Generative Models", Methodology; workload
+ * imbalance of static sequence sharding and whole-document sharding: the
+ * FlashCP abstract listed on the same page).
+ *  Work of query row i: n(i) = the keys it attends (causal: i - start of its
+ *  document + 1; otherwise its document's length). W(t) = sum_{i<t} n(i).
+ *  SP_CHUNK_EQUAL:        the RING token split.
+ *  SP_CHUNK_BALANCED:     bound r (0 < r < P) = the smallest t with
+ *                         P * W(t) >= r * W(T).
+ *  SP_CHUNK_BALANCED_DOC: the balanced bounds, for r = 1 .. P-1 in order:
+ *                         the document start nearest to bound r in work W
+ *                         (the earlier on a tie) replaces it when it moves at
+ *                         most W(T) / (16P) of work and lies after bound r-1;
+ *                         otherwise bound r is raised to bound r-1 if below.
+ *                         Fewer documents cut across ranks, each chunk within
+ *                         1/8 of the balanced work (plus one row).
+ *  cu_seqlens_host as sp_schedule_build. Chunks may be empty. */
+sp_status sp_chunk_bounds(int32_t mode, int32_t P, int32_t total_tokens, const int32_t* cu_seqlens_host,
+                          int32_t ndocs, int32_t causal, int32_t* out_bounds);
+
+/* sp_schedule_build_chunked — sp_schedule_build for RING or TASP with the
+ * chunks given by bounds[0..P] (bounds[0] = 0, bounds[P] = T, non-decreasing;
+ * NULL means SP_CHUNK_EQUAL). Rank r owns [bounds[r], bounds[r+1]); the KV
+ * chunks, TASP pieces and pruning follow the same rules. ZIGZAG takes only
+ * NULL (SP_ERR_UNSUPPORTED otherwise); bad bounds give SP_ERR_INVALID_ARG. */
+sp_status sp_schedule_build_chunked(sp_sched_kind kind, int32_t P, int32_t total_tokens,
+                                    const int32_t* cu_seqlens_host, int32_t ndocs, int32_t causal,
+                                    uint64_t seed, const int32_t* bounds, sp_item* out_items,
+                                    int64_t* inout_n_items);
+
 /* sp_tasp_cycles — host only. Writes the P-1 Hamiltonian cycles that TASP
  * schedules use for (P, seed) as successor tables: out_succ[c * P + u] is the
  * rank after u on ring c. out_succ must hold (P-1)*P int32. P = 1 writes

@@ -74,7 +74,10 @@ def _load():
         lib.oracle_check_schedule.restype = ctypes.c_int
         lib.oracle_check_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
                                               ctypes.c_int, ctypes.c_int, i32p, ctypes.c_longlong,
-                                              i32p, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
+                                              i32p, ctypes.c_int, ctypes.c_char_p, ctypes.c_int, i32p]
+        lib.oracle_chunk_bounds.restype = ctypes.c_int
+        lib.oracle_chunk_bounds.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                            ctypes.c_int, i32p]
         lib.oracle_link_bytes.restype = ctypes.c_int
         lib.oracle_link_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
                                           ctypes.c_int, i32p, ctypes.c_longlong, ctypes.c_int,
@@ -259,18 +262,35 @@ def check_hamiltonian(P: int, succ) -> int:
 
 
 def check_schedule(kind: int, P: int, T: int, cu_seqlens, causal: bool, items, succ=None,
-                   brute: bool = False):
-    """Returns (code, message); code 0 means every property holds."""
+                   brute: bool = False, bounds=None):
+    """Returns (code, message); code 0 means every property holds. bounds:
+    chunk boundaries [P+1] of a RING or TASP schedule (None: equal chunks)."""
     lib = _load()
     cu, cup = _i32(cu_seqlens)
     it, itp = _i32(np.asarray(items).reshape(-1, 8))
     if succ is None:
         succ = np.zeros((max(P - 1, 1), max(P, 1)), dtype=np.int32)
     sc, scp = _i32(succ)
+    bp = None
+    if bounds is not None:
+        bd, bp = _i32(bounds)
     buf = ctypes.create_string_buffer(256)
     rc = lib.oracle_check_schedule(kind, P, T, cup, len(cu) - 1, int(causal), itp, len(it), scp,
-                                   int(brute), buf, 256)
+                                   int(brute), buf, 256, bp)
     return int(rc), buf.value.decode()
+
+
+def chunk_bounds(mode: int, P: int, T: int, cu_seqlens, causal: bool):
+    """Chunk boundaries [P+1] of a chunking policy (0 equal, 1 balanced work,
+    2 balanced then moved onto document starts that are near in work)."""
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    out = np.zeros(P + 1, dtype=np.int32)
+    rc = lib.oracle_chunk_bounds(int(mode), int(P), int(T), cup, len(cu) - 1, int(causal),
+                                 out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    if rc != 0:
+        raise ValueError(f"oracle_chunk_bounds rejected its arguments (code {rc})")
+    return out
 
 
 def link_bytes(kind: int, P: int, T: int, cu_seqlens, causal: bool, succ=None,

@@ -29,6 +29,7 @@
 // hand-written schedule fixtures). No function here is unpinned.
 
 #include <cmath>
+#include <cstdlib>
 #include <cstdint>
 #include <cstring>
 #include <cstdio>
@@ -208,6 +209,66 @@ static void split_bounds(int n, int parts, int idx, int* b, int* e) {
   *e = *b + base + (idx < extra ? 1 : 0);
 }
 
+// Chunk boundaries out[0..P] of the chunking policies (load balancing,
+// "HSAP: A Hierarchical Sequence-aware Parallelism for Hybrid-Context
+// Generative Models", Methodology; whole-document sharding, FlashCP abstract
+// on the same page), written from their definitions with per-token loops:
+//   mode 0: the equal split above;
+//   mode 1: with n(i) the keys row i attends and W(t) = n(0) + ... + n(t-1),
+//           bound r = the smallest t with P * W(t) >= r * W(T);
+//   mode 2: the mode-1 bounds, then for r = 1 .. P-1 in order: the document
+//           start c (among cu[1 .. ndocs-1]) with |W(c) - W(bound r)| least
+//           (the smaller c on a tie) replaces bound r if 16 P |W(c) - W(bound r)|
+//           <= W(T) and c lies after the (already final) bound r-1; otherwise
+//           bound r is raised to bound r-1 if it is below it.
+// Returns 0, or nonzero for invalid arguments.
+int oracle_chunk_bounds(int mode, int P, int T, const int32_t* cu, int ndocs, int causal, int32_t* out) {
+  if (P < 1 || T < 0 || mode < 0 || mode > 2) return 1;
+  if (T == 0) {
+    for (int r = 0; r <= P; ++r) out[r] = 0;
+    return 0;
+  }
+  if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return 2;
+  if (mode == 0) {
+    for (int r = 0; r < P; ++r) {
+      int b, e;
+      split_bounds(T, P, r, &b, &e);
+      out[r] = b;
+    }
+    out[P] = T;
+    return 0;
+  }
+  std::vector<long long> W(static_cast<size_t>(T) + 1, 0);
+  for (int i = 0; i < T; ++i) {
+    const int D = doc_of(cu, ndocs, i);
+    const long long n = causal ? (i - cu[D] + 1) : (cu[D + 1] - cu[D]);
+    W[i + 1] = W[i] + n;
+  }
+  out[0] = 0;
+  for (int r = 1; r < P; ++r) {
+    int t = 0;
+    while (t < T && static_cast<long long>(P) * W[t] < static_cast<long long>(r) * W[T]) ++t;
+    out[r] = t;
+  }
+  out[P] = T;
+  if (mode == 2 && ndocs > 1) {
+    for (int r = 1; r < P; ++r) {
+      int best = -1;
+      long long bdist = 0;
+      for (int x = 1; x < ndocs; ++x) {
+        const long long dist = std::llabs(W[cu[x]] - W[out[r]]);
+        if (best < 0 || dist < bdist || (dist == bdist && cu[x] < best)) {
+          best = cu[x];
+          bdist = dist;
+        }
+      }
+      if (16LL * P * bdist <= W[T] && best > out[r - 1]) out[r] = best;
+      else if (out[r] < out[r - 1]) out[r] = out[r - 1];
+    }
+  }
+  return 0;
+}
+
 // Writes the expected RING (kind 0) or ZIGZAG (kind 1) item list, before and
 // after pruning of pairless items, in the canonical order: rank, then local Q
 // piece in token order, then step. Returns the number of items, or -1 when
@@ -303,13 +364,26 @@ int oracle_check_hamiltonian(int P, const int32_t* succ) {
 // counting every valid pair (use only for small T).
 int oracle_check_schedule(int kind, int P, int T, const int32_t* cu, int ndocs, int causal,
                           const int32_t* items, long long n_items, const int32_t* succ,
-                          int brute, char* msg, int msg_len) {
+                          int brute, char* msg, int msg_len, const int32_t* bounds) {
   auto fail = [&](int code, const char* fmt, long long a, long long b) {
     if (msg && msg_len > 0) std::snprintf(msg, msg_len, fmt, a, b);
     return code;
   };
   if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return fail(1, "bad cu_seqlens %lld %lld", 0, 0);
   if (P < 1) return fail(1, "bad P %lld %lld", P, 0);
+  if (bounds && (kind == 1 || bounds[0] != 0 || bounds[P] != T)) return fail(1, "bad bounds %lld %lld", kind, P);
+  if (bounds)
+    for (int r = 0; r < P; ++r)
+      if (bounds[r + 1] < bounds[r]) return fail(1, "bounds decrease at %lld %lld", r, bounds[r]);
+  // Chunk x of the RING / TASP split: the given bounds, else the equal split.
+  auto chunk_of = [&](int x, int* b, int* e) {
+    if (bounds) {
+      *b = bounds[x];
+      *e = bounds[x + 1];
+    } else {
+      split_bounds(T, P, x, b, e);
+    }
+  };
   // Owned Q ranges per rank.
   std::vector<std::vector<std::pair<int, int>>> own(P);
   for (int r = 0; r < P; ++r) {
@@ -320,8 +394,8 @@ int oracle_check_schedule(int kind, int P, int T, const int32_t* cu, int ndocs, 
       own[r].push_back({(2 * P - 1 - r) * c, (2 * P - r) * c});
     } else {
       int a, b;
-      split_bounds(T, P, r, &a, &b);
-      own[r].push_back({a, b});
+      chunk_of(r, &a, &b);
+      if (a < b) own[r].push_back({a, b});
     }
   }
   if (kind == 2 && P >= 2) {
@@ -354,13 +428,13 @@ int oracle_check_schedule(int kind, int P, int T, const int32_t* cu, int ndocs, 
     if (kind == 2) {
       int ea, eb;
       if (s == 0) {
-        split_bounds(T, P, r, &ea, &eb);
+        chunk_of(r, &ea, &eb);
       } else {
         if (P < 2 || c < 0 || c >= P - 1 || s >= P) return fail(6, "item %lld: bad step/cycle %lld", x, s);
         int src = r;
         for (int t = 0; t < s; ++t) src = pred[static_cast<size_t>(c) * P + src];
         int cb, ce;
-        split_bounds(T, P, src, &cb, &ce);
+        chunk_of(src, &cb, &ce);
         int pb, pe;
         split_bounds(ce - cb, P - 1, c, &pb, &pe);
         ea = cb + pb;

@@ -25,7 +25,7 @@ SP_DTYPE_BF16, SP_DTYPE_FP32 = 0, 1
 _STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_ERR_BUFFER_TOO_SMALL",
            4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_INTERNAL"}
 
-EXPORTED = ["sp_schedule_build", "sp_tasp_cycles", "sp_schedule_link_bytes", "sp_partial_attn", "sp_lse_merge",
+EXPORTED = ["sp_schedule_build", "sp_schedule_build_chunked", "sp_chunk_bounds", "sp_tasp_cycles", "sp_schedule_link_bytes", "sp_partial_attn", "sp_lse_merge",
             "sp_packed_attention_workspace_size", "sp_packed_attention",
             "sp_packed_attention_static_ws", "sp_packed_attention_backward_workspace_size",
             "sp_packed_attention_backward", "sp_check_device_status",
@@ -59,6 +59,11 @@ def load():
         lib.sp_schedule_build.restype = ctypes.c_int
         lib.sp_schedule_build.argtypes = [ctypes.c_int, i32, i32, vp, i32, i32, u64, vp,
                                           ctypes.POINTER(i64)]
+        lib.sp_schedule_build_chunked.restype = ctypes.c_int
+        lib.sp_schedule_build_chunked.argtypes = [ctypes.c_int, i32, i32, vp, i32, i32, u64, vp, vp,
+                                                  ctypes.POINTER(ctypes.c_int64)]
+        lib.sp_chunk_bounds.restype = ctypes.c_int
+        lib.sp_chunk_bounds.argtypes = [i32, i32, i32, vp, i32, i32, vp]
         lib.sp_tasp_cycles.restype = ctypes.c_int
         lib.sp_tasp_cycles.argtypes = [i32, u64, vp]
         lib.sp_schedule_link_bytes.restype = ctypes.c_int
@@ -104,19 +109,37 @@ def sp_status_string(code: int) -> str:
 # ----------------------------------------------------------------- host calls
 
 def sp_schedule_build(kind: int, P: int, total_tokens: int, cu_seqlens, causal: bool,
-                      seed: int = 0) -> np.ndarray:
-    """Items [n, 8] int32: rank, step, cycle, q_begin, q_end, kv_begin, kv_end, flags."""
+                      seed: int = 0, bounds=None) -> np.ndarray:
+    """Items [n, 8] int32: rank, step, cycle, q_begin, q_end, kv_begin, kv_end, flags.
+    bounds: chunk boundaries [P+1] for RING / TASP (sp_chunk_bounds); None = equal chunks."""
     lib = load()
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
     nd = len(cu) - 1
+    bd = None if bounds is None else np.ascontiguousarray(np.asarray(bounds, dtype=np.int32))
+    bp = None if bd is None else bd.ctypes.data
+    if bd is not None:
+        _need(bd.shape == (P + 1,), "bounds must hold P + 1 values")
     n = ctypes.c_int64(0)
-    _check(lib.sp_schedule_build(kind, P, total_tokens, cu.ctypes.data, nd, int(causal), seed, None,
-                                 ctypes.byref(n)), "sp_schedule_build")
+    _check(lib.sp_schedule_build_chunked(kind, P, total_tokens, cu.ctypes.data, nd, int(causal), seed,
+                                         bp, None, ctypes.byref(n)), "sp_schedule_build")
     out = np.zeros((max(n.value, 1), 8), dtype=np.int32)
     cap = ctypes.c_int64(n.value)
-    _check(lib.sp_schedule_build(kind, P, total_tokens, cu.ctypes.data, nd, int(causal), seed,
-                                 out.ctypes.data, ctypes.byref(cap)), "sp_schedule_build")
+    _check(lib.sp_schedule_build_chunked(kind, P, total_tokens, cu.ctypes.data, nd, int(causal), seed,
+                                         bp, out.ctypes.data, ctypes.byref(cap)), "sp_schedule_build")
     return out[:cap.value]
+
+
+SP_CHUNK_EQUAL, SP_CHUNK_BALANCED, SP_CHUNK_BALANCED_DOC = 0, 1, 2
+
+
+def sp_chunk_bounds(mode: int, P: int, total_tokens: int, cu_seqlens, causal: bool) -> np.ndarray:
+    """Chunk boundaries [P+1] of a chunking policy (SP_CHUNK_*)."""
+    lib = load()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    out = np.zeros(P + 1, dtype=np.int32)
+    _check(lib.sp_chunk_bounds(int(mode), int(P), int(total_tokens), cu.ctypes.data, len(cu) - 1,
+                               int(causal), out.ctypes.data), "sp_chunk_bounds")
+    return out
 
 
 def sp_tasp_cycles(P: int, seed: int = 0) -> np.ndarray:
@@ -303,13 +326,15 @@ class PackedAttention:
     sp_packed_attention. Only buffer management lives here."""
 
     def __init__(self, cu_seqlens, causal: bool, kind: int, P: int, Hq: int, seed: int = 0,
-                 device="cuda"):
+                 device="cuda", chunking: int = SP_CHUNK_EQUAL):
         torch = _torch()
         self.cu_host = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
         self.T = int(self.cu_host[-1])
         self.causal = bool(causal)
         self.kind, self.P, self.seed = kind, P, seed
-        self.items = sp_schedule_build(kind, P, self.T, self.cu_host, causal, seed)
+        self.bounds = (None if chunking == SP_CHUNK_EQUAL else
+                       sp_chunk_bounds(chunking, P, self.T, self.cu_host, causal))
+        self.items = sp_schedule_build(kind, P, self.T, self.cu_host, causal, seed, bounds=self.bounds)
         self.cu_dev = torch.from_numpy(self.cu_host).to(device)
         self.items_dev = torch.from_numpy(self.items).to(device)
         nbytes = sp_packed_attention_workspace_size(len(self.items))

@@ -18,6 +18,8 @@
 // not of the pages); every other P does.
 
 #include <algorithm>
+#include <cmath>
+#include <cstdlib>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -315,12 +317,117 @@ sp_status sp_tasp_cycles(int32_t P, uint64_t seed, int32_t* out_succ) {
   return SP_OK;
 }
 
+sp_status sp_chunk_bounds(int32_t mode, int32_t P, int32_t T, const int32_t* cu, int32_t ndocs,
+                          int32_t causal_i, int32_t* out) {
+  if (!out || P < 1 || T < 0) return SP_ERR_INVALID_ARG;
+  if (mode != SP_CHUNK_EQUAL && mode != SP_CHUNK_BALANCED && mode != SP_CHUNK_BALANCED_DOC)
+    return SP_ERR_INVALID_ARG;
+  if (T == 0) {
+    for (int r = 0; r <= P; ++r) out[r] = 0;
+    return SP_OK;
+  }
+  if (!valid_cu(cu, ndocs, T)) return SP_ERR_INVALID_ARG;
+  if (mode == SP_CHUNK_EQUAL) {
+    for (int r = 0; r < P; ++r) {
+      int b, e;
+      split_bounds(T, P, r, &b, &e);
+      out[r] = b;
+    }
+    out[P] = T;
+    return SP_OK;
+  }
+  const bool causal = causal_i != 0;
+  // Work of the first m rows of a document of length L (closed form per document).
+  auto doc_work = [&](int64_t m, int64_t L) { return causal ? m * (m + 1) / 2 : m * L; };
+  int64_t W = 0;
+  for (int d = 0; d < ndocs; ++d) W += doc_work(cu[d + 1] - cu[d], cu[d + 1] - cu[d]);
+  out[0] = 0;
+  int d = 0;
+  int64_t before = 0;  // work of the documents before d
+  for (int r = 1; r < P; ++r) {
+    // Smallest t with P * W(t) >= r * W: find the document, then the row in it.
+    const __int128 target = static_cast<__int128>(r) * W;
+    while (d < ndocs) {
+      const int64_t L = cu[d + 1] - cu[d];
+      if (static_cast<__int128>(P) * (before + doc_work(L, L)) >= target) break;
+      before += doc_work(L, L);
+      ++d;
+    }
+    if (d >= ndocs) {
+      out[r] = T;
+      continue;
+    }
+    const int64_t L = cu[d + 1] - cu[d];
+    auto ok = [&](int64_t m) { return static_cast<__int128>(P) * (before + doc_work(m, L)) >= target; };
+    // Initial guess, then exact correction with integer checks.
+    const double need = (static_cast<double>(target) / P) - static_cast<double>(before);
+    int64_t m = causal ? static_cast<int64_t>(std::ceil((std::sqrt(1.0 + 8.0 * std::max(need, 0.0)) - 1.0) / 2.0))
+                       : static_cast<int64_t>(std::ceil(std::max(need, 0.0) / static_cast<double>(L)));
+    m = std::min<int64_t>(std::max<int64_t>(m, 0), L);
+    while (m > 0 && ok(m - 1)) --m;
+    while (m < L && !ok(m)) ++m;
+    out[r] = cu[d] + static_cast<int32_t>(m);
+  }
+  out[P] = T;
+  for (int r = 1; r <= P; ++r) out[r] = std::max(out[r], out[r - 1]);
+  if (mode == SP_CHUNK_BALANCED_DOC && ndocs > 1) {
+    // Work before each document start, and W(t) for any t.
+    std::vector<int64_t> Wd(static_cast<size_t>(ndocs) + 1, 0);
+    for (int x = 0; x < ndocs; ++x) Wd[x + 1] = Wd[x] + doc_work(cu[x + 1] - cu[x], cu[x + 1] - cu[x]);
+    auto work_at = [&](int t) {
+      const int x = static_cast<int>(std::upper_bound(cu, cu + ndocs + 1, t) - cu) - 1;
+      if (x >= ndocs) return Wd[ndocs];
+      return Wd[x] + doc_work(t - cu[x], cu[x + 1] - cu[x]);
+    };
+    for (int r = 1; r < P; ++r) {
+      // The document start (cu[1 .. ndocs-1]) nearest in work to bound r: one
+      // of the two around it, the earlier on a tie.
+      const int64_t wb = work_at(out[r]);
+      const int32_t* hi = std::lower_bound(cu + 1, cu + ndocs, out[r]);
+      int best = -1;
+      int64_t bdist = 0;
+      for (const int32_t* c : {hi - 1, hi}) {
+        if (c < cu + 1 || c >= cu + ndocs) continue;
+        const int64_t dist = std::llabs(Wd[c - cu] - wb);
+        if (best < 0 || dist < bdist) {
+          best = *c;
+          bdist = dist;
+        }
+      }
+      if (best >= 0 && static_cast<__int128>(bdist) * 16 * P <= W && best > out[r - 1]) out[r] = best;
+      else out[r] = std::max(out[r], out[r - 1]);
+    }
+  }
+  return SP_OK;
+}
+
 sp_status sp_schedule_build(sp_sched_kind kind, int32_t P, int32_t T, const int32_t* cu,
                             int32_t ndocs, int32_t causal_i, uint64_t seed, sp_item* out,
                             int64_t* inout_n) {
+  return sp_schedule_build_chunked(kind, P, T, cu, ndocs, causal_i, seed, nullptr, out, inout_n);
+}
+
+sp_status sp_schedule_build_chunked(sp_sched_kind kind, int32_t P, int32_t T, const int32_t* cu,
+                                    int32_t ndocs, int32_t causal_i, uint64_t seed,
+                                    const int32_t* bounds, sp_item* out, int64_t* inout_n) {
   if (!inout_n || P < 1 || T < 0) return SP_ERR_INVALID_ARG;
   if (kind != SP_SCHED_RING && kind != SP_SCHED_ZIGZAG && kind != SP_SCHED_TASP)
     return SP_ERR_INVALID_ARG;
+  if (bounds && kind == SP_SCHED_ZIGZAG) return SP_ERR_UNSUPPORTED;
+  if (bounds) {
+    if (bounds[0] != 0 || bounds[P] != T) return SP_ERR_INVALID_ARG;
+    for (int r = 0; r < P; ++r)
+      if (bounds[r + 1] < bounds[r]) return SP_ERR_INVALID_ARG;
+  }
+  // Chunk x of the RING / TASP split.
+  auto chunk = [&](int x, int* b, int* e) {
+    if (bounds) {
+      *b = bounds[x];
+      *e = bounds[x + 1];
+    } else {
+      split_bounds(T, P, x, b, e);
+    }
+  };
   if (T == 0) {
     if (ndocs != 0 || (cu && cu[0] != 0)) return SP_ERR_INVALID_ARG;
     *inout_n = 0;
@@ -352,10 +459,10 @@ sp_status sp_schedule_build(sp_sched_kind kind, int32_t P, int32_t T, const int3
   for (int r = 0; r < P; ++r) {
     if (kind == SP_SCHED_RING) {
       int qa, qb;
-      split_bounds(T, P, r, &qa, &qb);
+      chunk(r, &qa, &qb);
       for (int s = 0; s < P; ++s) {
         int ka, kb;
-        split_bounds(T, P, ((r - s) % P + P) % P, &ka, &kb);
+        chunk(((r - s) % P + P) % P, &ka, &kb);
         emit(r, s, 0, qa, qb, ka, kb);
       }
     } else if (kind == SP_SCHED_ZIGZAG) {
@@ -370,14 +477,14 @@ sp_status sp_schedule_build(sp_sched_kind kind, int32_t P, int32_t T, const int3
         }
     } else {
       int qa, qb;
-      split_bounds(T, P, r, &qa, &qb);
+      chunk(r, &qa, &qb);
       emit(r, 0, 0, qa, qb, qa, qb);
       for (int t = 1; t < P; ++t)
         for (int c = 0; c < P - 1; ++c) {
           int src = r;
           for (int h = 0; h < t; ++h) src = pred[static_cast<size_t>(c) * P + src];
           int cb, ce, pb, pe;
-          split_bounds(T, P, src, &cb, &ce);
+          chunk(src, &cb, &ce);
           split_bounds(ce - cb, P - 1, c, &pb, &pe);
           emit(r, t, c, qa, qb, cb + pb, cb + pe);
         }
