@@ -399,6 +399,96 @@ def kernel_only(args, local):
                       "tflops": flop / (ms * 1e-3) / 1e12}), flush=True)
 
 
+def balance_report(args, local):
+    """Per-virtual-rank device time of each chunking policy: every rank's items
+    run alone through sp_packed_attention (one persistent launch on the whole
+    GPU), so the slowest rank is the compute critical path of one SP step on P
+    GPUs (transfers not included). Packed workloads and the single causal
+    document, with the policies the schedule kind allows."""
+    import torch
+    import sequence_blockwise_gb300 as sb
+    from sequence_blockwise_gb300 import workloads as wl
+    dev = torch.device("cuda", local)
+    cases = [(1, sb.SP_SCHED_ZIGZAG, [0]), (1, sb.SP_SCHED_RING, [0, 1]),
+             (2, sb.SP_SCHED_TASP, [0, 1, 2]), (4, sb.SP_SCHED_TASP, [0, 1, 2])]
+    out = []
+    for idx, kind, modes in cases:
+        w = wl.WORKLOADS[idx]
+        cu = wl.cu_seqlens(w)
+        q, k, v = wl.make_qkv(w, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
+        cu_dev = torch.from_numpy(cu).to(dev)
+        for mode in modes:
+            bounds = None if mode == 0 else sb.sp_chunk_bounds(mode, w.P, w.T, cu, w.causal)
+            items = sb.sp_schedule_build(kind, w.P, w.T, cu, w.causal, seed=w.seed, bounds=bounds)
+            ms, pairs = [], []
+            for r in range(w.P):
+                mine = np.ascontiguousarray(items[items[:, 0] == r])
+                pr = sum(valid_pairs_range(cu, w.causal, it) for it in mine)
+                pairs.append(pr)
+                if len(mine) == 0:
+                    ms.append(0.0)
+                    continue
+                it_dev = torch.from_numpy(mine).to(dev)
+                ws = torch.empty(sb.sp_packed_attention_workspace_size(len(mine)), dtype=torch.uint8,
+                                 device=dev)
+                run = lambda: sb.sp_packed_attention(q, k, v, o, lse, cu_dev, w.causal, it_dev, ws)
+                run()
+                torch.cuda.synchronize(dev)
+                t = []
+                for _ in range(3):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    run()
+                    b.record()
+                    torch.cuda.synchronize(dev)
+                    t.append(a.elapsed_time(b))
+                ms.append(float(np.median(t)))
+            sb.sp_check_device_status()
+            ms_a, pr_a = np.array(ms), np.array(pairs, dtype=np.float64)
+            cuts = 0 if bounds is None else int(sum(1 for x in bounds[1:-1] if x not in set(cu.tolist())))
+            out.append({"workload": w.name, "schedule": sched_name(kind), "P_virtual": w.P,
+                        "chunking": ["equal", "balanced", "balanced_doc"][mode], "n_items": int(len(items)),
+                        "bounds_inside_documents": cuts,
+                        "pairs_max_over_mean": round(float(pr_a.max() / pr_a.mean()), 4),
+                        "rank_ms_max": round(float(ms_a.max()), 4), "rank_ms_mean": round(float(ms_a.mean()), 4),
+                        "rank_ms_max_over_mean": round(float(ms_a.max() / ms_a.mean()), 4),
+                        "rank_ms": [round(x, 3) for x in ms]})
+            print(json.dumps(out[-1]), flush=True)
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+    return out
+
+
+def valid_pairs_range(cu, causal, it):
+    """Valid (query, key) pairs of one item (closed form per document)."""
+    qa, qb, ka, kb = int(it[3]), int(it[4]), int(it[5]), int(it[6])
+    total = 0
+    for d in range(len(cu) - 1):
+        a, b = int(cu[d]), int(cu[d + 1])
+        q0, q1 = max(a, qa), min(b, qb)
+        k0, k1 = max(a, ka), min(b, kb)
+        if q0 >= q1 or k0 >= k1:
+            continue
+        if not causal:
+            total += (q1 - q0) * (k1 - k0)
+            continue
+        # sum over rows i in [q0, q1) of max(0, min(k1, i + 1) - k0)
+        for_rows_lo = max(q0, k0)
+        if for_rows_lo >= q1:
+            continue
+        # rows with i + 1 <= k1: count i + 1 - k0; rows with i + 1 > k1: k1 - k0
+        m1 = min(q1, k1)  # rows i < m1 have i + 1 <= k1
+        if m1 > for_rows_lo:
+            n = m1 - for_rows_lo
+            first = for_rows_lo + 1 - k0
+            total += n * first + n * (n - 1) // 2
+        if q1 > max(m1, for_rows_lo):
+            total += (q1 - max(m1, for_rows_lo)) * (k1 - k0)
+    return total
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,6 +502,8 @@ def main():
                     help="skip the backward measurement reported beside the headline")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
                     help="with --kernel-only: which pass to run")
+    ap.add_argument("--balance", action="store_true",
+                    help="per-virtual-rank device time of the chunking policies (one JSON line each)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only W warm-up + K device-resident steps (driver for ncu captures)")
     args = ap.parse_args()
@@ -454,6 +546,9 @@ def main():
 
     if args.kernel_only:
         kernel_only(args, local)
+        return
+    if args.balance:
+        balance_report(args, local)
         return
 
     result, w, cu = run_ours(args, world, rank, local)

@@ -52,3 +52,23 @@ def test_valid_pair_count_closed_form():
     cu = np.array([0, 100, 256])
     assert bench.valid_pairs(cu, True) == 100 * 101 // 2 + 156 * 157 // 2
     assert bench.valid_pairs(cu, False) == 100 * 100 + 156 * 156
+
+
+def test_item_pair_count_matches_oracle():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import oracle
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        T = int(rng.integers(1, 200))
+        nd = int(rng.integers(1, min(T, 6) + 1))
+        cuts = np.sort(rng.choice(np.arange(1, T), size=nd - 1, replace=False)) if nd > 1 else []
+        cu = np.concatenate([[0], cuts, [T]]).astype(np.int32)
+        qa = int(rng.integers(0, T))
+        qb = int(rng.integers(qa + 1, T + 1))
+        ka = int(rng.integers(0, T))
+        kb = int(rng.integers(ka + 1, T + 1))
+        for causal in (True, False):
+            assert bench.valid_pairs_range(cu, causal, [0, 0, 0, qa, qb, ka, kb]) == \
+                oracle.valid_pairs(cu, causal, qa, qb, ka, kb)
