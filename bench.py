@@ -409,10 +409,12 @@ def balance_report(args, local):
     import sequence_blockwise_gb300 as sb
     from sequence_blockwise_gb300 import workloads as wl
     dev = torch.device("cuda", local)
-    cases = [(1, sb.SP_SCHED_ZIGZAG, [0]), (1, sb.SP_SCHED_RING, [0, 1]),
-             (2, sb.SP_SCHED_TASP, [0, 1, 2]), (4, sb.SP_SCHED_TASP, [0, 1, 2])]
+    # (workload, schedule kind, chunking policies, Ulysses ranks per group)
+    cases = [(1, sb.SP_SCHED_ZIGZAG, [0], 1), (1, sb.SP_SCHED_RING, [0, 1], 1),
+             (2, sb.SP_SCHED_TASP, [0, 1, 2], 1), (4, sb.SP_SCHED_TASP, [0, 1, 2], 1),
+             (3, sb.SP_SCHED_RING, [0], 1), (3, sb.SP_SCHED_RING, [0], 8), (1, sb.SP_SCHED_ZIGZAG, [0], 4)]
     out = []
-    for idx, kind, modes in cases:
+    for idx, kind, modes, U in cases:
         w = wl.WORKLOADS[idx]
         cu = wl.cu_seqlens(w)
         q, k, v = wl.make_qkv(w, dev)
@@ -420,20 +422,29 @@ def balance_report(args, local):
         lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
         cu_dev = torch.from_numpy(cu).to(dev)
         for mode in modes:
-            bounds = None if mode == 0 else sb.sp_chunk_bounds(mode, w.P, w.T, cu, w.causal)
-            items = sb.sp_schedule_build(kind, w.P, w.T, cu, w.causal, seed=w.seed, bounds=bounds)
+            R = w.P // U
+            bounds = None if mode == 0 else sb.sp_chunk_bounds(mode, R, w.T, cu, w.causal)
+            if U > 1:
+                items, heads = sb.sp_schedule_build_hier(kind, R, U, w.T, cu, w.causal, w.Hq, seed=w.seed,
+                                                         bounds=bounds)
+            else:
+                items = sb.sp_schedule_build(kind, w.P, w.T, cu, w.causal, seed=w.seed, bounds=bounds)
+                heads = np.tile(np.array([[0, w.Hq]], dtype=np.int32), (len(items), 1))
             ms, pairs = [], []
             for r in range(w.P):
-                mine = np.ascontiguousarray(items[items[:, 0] == r])
-                pr = sum(valid_pairs_range(cu, w.causal, it) for it in mine)
+                sel = items[:, 0] == r
+                mine = np.ascontiguousarray(items[sel])
+                hmine = np.ascontiguousarray(heads[sel])
+                pr = sum(valid_pairs_range(cu, w.causal, it) * int(h[1] - h[0]) for it, h in zip(mine, hmine))
                 pairs.append(pr)
                 if len(mine) == 0:
                     ms.append(0.0)
                     continue
                 it_dev = torch.from_numpy(mine).to(dev)
+                hd_dev = torch.from_numpy(hmine).to(dev)
                 ws = torch.empty(sb.sp_packed_attention_workspace_size(len(mine)), dtype=torch.uint8,
                                  device=dev)
-                run = lambda: sb.sp_packed_attention(q, k, v, o, lse, cu_dev, w.causal, it_dev, ws)
+                run = lambda: sb.sp_packed_attention_ex(q, k, v, o, lse, cu_dev, w.causal, it_dev, hd_dev, ws)
                 run()
                 torch.cuda.synchronize(dev)
                 t = []
@@ -448,7 +459,8 @@ def balance_report(args, local):
             sb.sp_check_device_status()
             ms_a, pr_a = np.array(ms), np.array(pairs, dtype=np.float64)
             cuts = 0 if bounds is None else int(sum(1 for x in bounds[1:-1] if x not in set(cu.tolist())))
-            out.append({"workload": w.name, "schedule": sched_name(kind), "P_virtual": w.P,
+            out.append({"workload": w.name, "schedule": sched_name(kind) + (f" {R}x{U} (head split)" if U > 1 else ""),
+                        "P_virtual": w.P,
                         "chunking": ["equal", "balanced", "balanced_doc"][mode], "n_items": int(len(items)),
                         "bounds_inside_documents": cuts,
                         "pairs_max_over_mean": round(float(pr_a.max() / pr_a.mean()), 4),

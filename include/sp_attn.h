@@ -142,6 +142,28 @@ sp_status sp_schedule_build_chunked(sp_sched_kind kind, int32_t P, int32_t total
                                     uint64_t seed, const int32_t* bounds, sp_item* out_items,
                                     int64_t* inout_n_items);
 
+/* sp_schedule_build_hier — host only; a two-level schedule on P = R * U
+ * virtual ranks ("HSAP: A Hierarchical Sequence-aware Parallelism for
+ * Hybrid-Context Generative Models", abstract and Methodology: Inter-SP
+ * between device groups combined with Intra-SP inside a group; the Intra-SP
+ * level read as a Ulysses-style head split, DeepSpeed-Ulysses being the
+ * Intra-SP scheme the page compares with).
+ *  The R groups run the Inter-SP schedule `inter_kind` (RING, ZIGZAG or TASP
+ *  over R group chunks, chunk bounds as sp_schedule_build_chunked, NULL for
+ *  equal). Inside group g the U ranks split the query heads: rank g*U + u
+ *  holds group g's whole Q chunk and the key/value chunks group g visits, for
+ *  query heads [u Hq/U, (u+1) Hq/U) (Hq % U == 0). Every item of the R-group
+ *  schedule appears once per u, in rank order.
+ *  out_items / out_heads (int32 [n][2], the items' query-head ranges) follow
+ *  the two-call protocol of sp_schedule_build (out_items == NULL: count only).
+ *  Run the result with sp_packed_attention_ex; its head ranges must then
+ *  cover whole groups of Hq/Hkv heads or lie inside one (Hkv % U == 0, or
+ *  Hq/U divides Hq/Hkv). */
+sp_status sp_schedule_build_hier(sp_sched_kind inter_kind, int32_t R, int32_t U, int32_t total_tokens,
+                                 const int32_t* cu_seqlens_host, int32_t ndocs, int32_t causal,
+                                 uint64_t seed, int32_t Hq, const int32_t* bounds, sp_item* out_items,
+                                 int32_t* out_heads, int64_t* inout_n_items);
+
 /* sp_tasp_cycles — host only. Writes the P-1 Hamiltonian cycles that TASP
  * schedules use for (P, seed) as successor tables: out_succ[c * P + u] is the
  * rank after u on ring c. out_succ must hold (P-1)*P int32. P = 1 writes
@@ -223,6 +245,27 @@ sp_status sp_packed_attention(const void* q, const void* k, const void* v, void*
                               const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal, float scale,
                               const sp_item* items_dev, int64_t n_items, void* workspace,
                               size_t workspace_bytes, void* stream);
+
+/* sp_packed_attention_ex — sp_packed_attention over items that each cover a
+ * range of query heads, as hierarchical schedules produce (an Intra-SP head
+ * split under an Inter-SP ring: "HSAP: A Hierarchical Sequence-aware
+ * Parallelism for Hybrid-Context Generative Models", abstract and
+ * Methodology; see sp_schedule_build_hier).
+ *  item_heads_dev: device int32 [n_items][2], query heads [h_begin, h_end) of
+ *     each item (NULL: all heads, which is sp_packed_attention). A range must
+ *     cover whole groups of Hq/Hkv query heads or lie inside one group.
+ *     Items that share a rank, Q range and head range must be contiguous;
+ *     the (Q range x head range) rectangles of different groups must not
+ *     overlap. Violations are reported through sp_check_device_status
+ *     (SP_ERR_INTERNAL, nothing written).
+ *  Other arguments as sp_packed_attention; rows and heads no item covers are
+ *  not written. */
+sp_status sp_packed_attention_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,
+                                 const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal,
+                                 float scale, const sp_item* items_dev, const int32_t* item_heads_dev,
+                                 int64_t n_items, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /* sp_packed_attention_static_ws — sp_packed_attention for callers that cannot
  * allocate device memory. The pages have no counterpart to this call.

@@ -75,6 +75,11 @@ def _load():
         lib.oracle_check_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
                                               ctypes.c_int, ctypes.c_int, i32p, ctypes.c_longlong,
                                               i32p, ctypes.c_int, ctypes.c_char_p, ctypes.c_int, i32p]
+        lib.oracle_check_hier_schedule.restype = ctypes.c_int
+        lib.oracle_check_hier_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, i32p,
+                                                   i32p, ctypes.c_longlong, i32p, ctypes.c_int,
+                                                   ctypes.c_char_p, ctypes.c_int, i32p]
         lib.oracle_chunk_bounds.restype = ctypes.c_int
         lib.oracle_chunk_bounds.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
                                             ctypes.c_int, i32p]
@@ -277,6 +282,25 @@ def check_schedule(kind: int, P: int, T: int, cu_seqlens, causal: bool, items, s
     buf = ctypes.create_string_buffer(256)
     rc = lib.oracle_check_schedule(kind, P, T, cup, len(cu) - 1, int(causal), itp, len(it), scp,
                                    int(brute), buf, 256, bp)
+    return int(rc), buf.value.decode()
+
+
+def check_hier_schedule(kind: int, R: int, U: int, Hq: int, T: int, cu_seqlens, causal: bool, items, heads,
+                        succ=None, brute: bool = False, bounds=None):
+    """Two-level schedule check; returns (code, message), 0 when every property holds."""
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    it, itp = _i32(np.asarray(items).reshape(-1, 8))
+    hd, hdp = _i32(np.asarray(heads).reshape(-1, 2))
+    if succ is None:
+        succ = np.zeros((max(R - 1, 1), max(R, 1)), dtype=np.int32)
+    sc, scp = _i32(succ)
+    bp = None
+    if bounds is not None:
+        bd, bp = _i32(bounds)
+    buf = ctypes.create_string_buffer(256)
+    rc = lib.oracle_check_hier_schedule(kind, R, U, Hq, T, cup, len(cu) - 1, int(causal), itp, hdp, len(it),
+                                        scp, int(brute), buf, 256, bp)
     return int(rc), buf.value.decode()
 
 

@@ -492,6 +492,49 @@ int oracle_check_schedule(int kind, int P, int T, const int32_t* cu, int ndocs, 
   return 0;
 }
 
+// Checks a two-level schedule on P = R * U ranks (Inter-SP schedule of kind
+// `kind` over R groups; inside group g, rank g*U + u takes query heads
+// [u Hq/U, (u+1) Hq/U)): every item's head range must be its rank's slice,
+// and for each u the items of ranks g*U + u, renumbered g, must form a valid
+// R-rank schedule by oracle_check_schedule (same succ, bounds and brute
+// options). Then every (query, key, head) triple the mask allows is covered
+// exactly once: each head lies in exactly one slice, and within a slice the
+// R-rank schedule covers every valid pair once. Returns 0 or a nonzero code
+// (20 bad arguments, 21 bad rank, 22 wrong head range, 30 + the code of the
+// failing slice's check).
+int oracle_check_hier_schedule(int kind, int R, int U, int Hq, int T, const int32_t* cu, int ndocs,
+                               int causal, const int32_t* items, const int32_t* heads, long long n_items,
+                               const int32_t* succ, int brute, char* msg, int msg_len,
+                               const int32_t* bounds) {
+  auto fail = [&](int code, const char* fmt, long long a, long long b) {
+    if (msg && msg_len > 0) std::snprintf(msg, msg_len, fmt, a, b);
+    return code;
+  };
+  if (R < 1 || U < 1 || Hq < 1 || Hq % U != 0) return fail(20, "bad R/U/Hq %lld %lld", R, U);
+  const int hs = Hq / U;
+  std::vector<std::vector<int32_t>> slice(U);
+  for (long long x = 0; x < n_items; ++x) {
+    const int32_t* it = items + x * 8;
+    const int r = it[0];
+    if (r < 0 || r >= R * U) return fail(21, "item %lld: bad rank %lld", x, r);
+    const int u = r % U;
+    if (heads[2 * x] != u * hs || heads[2 * x + 1] != (u + 1) * hs)
+      return fail(22, "item %lld: head range starts at %lld", x, heads[2 * x]);
+    for (int c = 0; c < 8; ++c) slice[u].push_back(c == 0 ? r / U : it[c]);
+  }
+  for (int u = 0; u < U; ++u) {
+    const long long m = static_cast<long long>(slice[u].size() / 8);
+    char sub[200];
+    const int rc = oracle_check_schedule(kind, R, T, cu, ndocs, causal, slice[u].data(), m, succ, brute, sub,
+                                         sizeof sub, bounds);
+    if (rc != 0) {
+      if (msg && msg_len > 0) std::snprintf(msg, msg_len, "head slice %d: %s", u, sub);
+      return 30 + rc;
+    }
+  }
+  return 0;
+}
+
 // Gradients of the masked attention (the backward of the operation above):
 // with P_ij = exp(s_ij - LSE_i) over the valid keys j of query i,
 //   dV_j  = sum_i P_ij dO_i,              dP_ij = dO_i . v_j,

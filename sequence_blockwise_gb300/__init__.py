@@ -25,7 +25,8 @@ SP_DTYPE_BF16, SP_DTYPE_FP32 = 0, 1
 _STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_ERR_BUFFER_TOO_SMALL",
            4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_INTERNAL"}
 
-EXPORTED = ["sp_schedule_build", "sp_schedule_build_chunked", "sp_chunk_bounds", "sp_tasp_cycles", "sp_schedule_link_bytes", "sp_partial_attn", "sp_lse_merge",
+EXPORTED = ["sp_schedule_build", "sp_schedule_build_chunked", "sp_schedule_build_hier", "sp_chunk_bounds",
+            "sp_tasp_cycles", "sp_packed_attention_ex", "sp_schedule_link_bytes", "sp_partial_attn", "sp_lse_merge",
             "sp_packed_attention_workspace_size", "sp_packed_attention",
             "sp_packed_attention_static_ws", "sp_packed_attention_backward_workspace_size",
             "sp_packed_attention_backward", "sp_check_device_status",
@@ -62,6 +63,12 @@ def load():
         lib.sp_schedule_build_chunked.restype = ctypes.c_int
         lib.sp_schedule_build_chunked.argtypes = [ctypes.c_int, i32, i32, vp, i32, i32, u64, vp, vp,
                                                   ctypes.POINTER(ctypes.c_int64)]
+        lib.sp_schedule_build_hier.restype = ctypes.c_int
+        lib.sp_schedule_build_hier.argtypes = [ctypes.c_int, i32, i32, i32, vp, i32, i32, u64, i32, vp, vp,
+                                               vp, ctypes.POINTER(ctypes.c_int64)]
+        lib.sp_packed_attention_ex.restype = ctypes.c_int
+        lib.sp_packed_attention_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int,
+                                               vp, i32, i32, f32, vp, vp, i64, vp, ctypes.c_size_t, vp]
         lib.sp_chunk_bounds.restype = ctypes.c_int
         lib.sp_chunk_bounds.argtypes = [i32, i32, i32, vp, i32, i32, vp]
         lib.sp_tasp_cycles.restype = ctypes.c_int
@@ -127,6 +134,26 @@ def sp_schedule_build(kind: int, P: int, total_tokens: int, cu_seqlens, causal: 
     _check(lib.sp_schedule_build_chunked(kind, P, total_tokens, cu.ctypes.data, nd, int(causal), seed,
                                          bp, out.ctypes.data, ctypes.byref(cap)), "sp_schedule_build")
     return out[:cap.value]
+
+
+def sp_schedule_build_hier(inter_kind: int, R: int, U: int, total_tokens: int, cu_seqlens, causal: bool,
+                           Hq: int, seed: int = 0, bounds=None):
+    """Two-level schedule on R x U virtual ranks: (items [n, 8], heads [n, 2])."""
+    lib = load()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    nd = len(cu) - 1
+    bd = None if bounds is None else np.ascontiguousarray(np.asarray(bounds, dtype=np.int32))
+    bp = None if bd is None else bd.ctypes.data
+    n = ctypes.c_int64(0)
+    _check(lib.sp_schedule_build_hier(inter_kind, R, U, total_tokens, cu.ctypes.data, nd, int(causal), seed,
+                                      Hq, bp, None, None, ctypes.byref(n)), "sp_schedule_build_hier")
+    items = np.zeros((max(n.value, 1), 8), dtype=np.int32)
+    heads = np.zeros((max(n.value, 1), 2), dtype=np.int32)
+    cap = ctypes.c_int64(n.value)
+    _check(lib.sp_schedule_build_hier(inter_kind, R, U, total_tokens, cu.ctypes.data, nd, int(causal), seed,
+                                      Hq, bp, items.ctypes.data, heads.ctypes.data, ctypes.byref(cap)),
+           "sp_schedule_build_hier")
+    return items[:cap.value], heads[:cap.value]
 
 
 SP_CHUNK_EQUAL, SP_CHUNK_BALANCED, SP_CHUNK_BALANCED_DOC = 0, 1, 2
@@ -259,6 +286,28 @@ def sp_packed_attention(q, k, v, o, lse, cu_seqlens, causal: bool, items_dev, wo
                                       _stream(stream)), "sp_packed_attention")
 
 
+def sp_packed_attention_ex(q, k, v, o, lse, cu_seqlens, causal: bool, items_dev, heads_dev, workspace,
+                           scale: float | None = None, stream=None):
+    """sp_packed_attention over items with query-head ranges (heads_dev: int32 [n, 2] on device)."""
+    T, Hq, Hkv, d = _check_qkv(q, k, v)
+    torch = _torch()
+    _need(o.dtype == q.dtype and tuple(o.shape) == (T, Hq, d) and o.is_contiguous(), "o: [T, Hq, d]")
+    _need(lse.dtype == torch.float32 and tuple(lse.shape) == (Hq, T) and lse.is_contiguous(),
+          "lse must be fp32 [Hq, T]")
+    _need(items_dev.dtype == torch.int32 and items_dev.is_cuda and items_dev.dim() == 2 and
+          items_dev.shape[1] == 8 and items_dev.is_contiguous(), "items_dev: int32 [n, 8] on device")
+    _need(heads_dev.dtype == torch.int32 and heads_dev.is_cuda and tuple(heads_dev.shape) == (items_dev.shape[0], 2)
+          and heads_dev.is_contiguous(), "heads_dev: int32 [n, 2] on device")
+    _need(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_cuda, "cu_seqlens must be int32 on device")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    _check(load().sp_packed_attention_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, Hq, Hkv, d,
+                                         _dtype_code(q), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+                                         int(causal), scale, _ptr(items_dev), _ptr(heads_dev),
+                                         items_dev.shape[0], _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream)),
+           "sp_packed_attention_ex")
+
+
 def sp_packed_attention_static_ws(q, k, v, o, lse, cu_seqlens, causal: bool, items_dev,
                                   scale: float | None = None, stream=None):
     """sp_packed_attention without a caller workspace, for callers that cannot
@@ -326,17 +375,28 @@ class PackedAttention:
     sp_packed_attention. Only buffer management lives here."""
 
     def __init__(self, cu_seqlens, causal: bool, kind: int, P: int, Hq: int, seed: int = 0,
-                 device="cuda", chunking: int = SP_CHUNK_EQUAL):
+                 device="cuda", chunking: int = SP_CHUNK_EQUAL, ulysses: int = 1):
+        """ulysses > 1: two-level schedule, P / ulysses groups running `kind`
+        between them and a query-head split over `ulysses` ranks inside each."""
         torch = _torch()
         self.cu_host = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
         self.T = int(self.cu_host[-1])
         self.causal = bool(causal)
         self.kind, self.P, self.seed = kind, P, seed
+        self.ulysses = int(ulysses)
+        _need(self.ulysses >= 1 and P % self.ulysses == 0, "P must be a multiple of ulysses")
+        groups = P // self.ulysses
         self.bounds = (None if chunking == SP_CHUNK_EQUAL else
-                       sp_chunk_bounds(chunking, P, self.T, self.cu_host, causal))
-        self.items = sp_schedule_build(kind, P, self.T, self.cu_host, causal, seed, bounds=self.bounds)
+                       sp_chunk_bounds(chunking, groups, self.T, self.cu_host, causal))
+        self.heads = None
+        if self.ulysses > 1:
+            self.items, self.heads = sp_schedule_build_hier(kind, groups, self.ulysses, self.T, self.cu_host,
+                                                            causal, Hq, seed, bounds=self.bounds)
+        else:
+            self.items = sp_schedule_build(kind, P, self.T, self.cu_host, causal, seed, bounds=self.bounds)
         self.cu_dev = torch.from_numpy(self.cu_host).to(device)
         self.items_dev = torch.from_numpy(self.items).to(device)
+        self.heads_dev = None if self.heads is None else torch.from_numpy(self.heads).to(device)
         nbytes = sp_packed_attention_workspace_size(len(self.items))
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
 
@@ -347,13 +407,18 @@ class PackedAttention:
             o = torch.empty_like(q)
         if lse is None:
             lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
-        sp_packed_attention(q, k, v, o, lse, self.cu_dev, self.causal, self.items_dev, self.workspace,
-                            scale=scale, stream=stream)
+        if self.heads_dev is not None:
+            sp_packed_attention_ex(q, k, v, o, lse, self.cu_dev, self.causal, self.items_dev, self.heads_dev,
+                                   self.workspace, scale=scale, stream=stream)
+        else:
+            sp_packed_attention(q, k, v, o, lse, self.cu_dev, self.causal, self.items_dev, self.workspace,
+                                scale=scale, stream=stream)
         return o, lse
 
     def backward(self, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale=None, stream=None):
         """Gradients (dq, dk, dv) of the forward call that returned (o, lse)."""
         torch = _torch()
+        _need(self.heads is None, "the backward takes schedules without a head split")
         T, Hq, d = q.shape
         nbytes = sp_packed_attention_backward_workspace_size(len(self.items), T, Hq)
         if getattr(self, "bwd_workspace", None) is None or self.bwd_workspace.numel() < nbytes:

@@ -167,7 +167,7 @@ sp_status sp_partial_attn(const void* q, const void* k, const void* v, float* o_
   a.segs = nullptr;
   a.header = nullptr;
   a.inline_item = sp_item{0, 0, 0, q_begin, q_end, kv_begin, kv_end, 0};
-  a.inline_seg = sp::SegEntry{q_begin, q_end, 0, 1, 0, qg, 0, 0};
+  a.inline_seg = sp::SegEntry{q_begin, q_end, 0, 1, 0, qg, 0, Hq};
   a.inline_n_units = qg * Hq;
   a.rows_per_unit = rpu;
   a.out_mode = 1;
@@ -202,6 +202,16 @@ sp_status sp_packed_attention(const void* q, const void* k, const void* v, void*
                               const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal, float scale,
                               const sp_item* items_dev, int64_t n_items, void* workspace,
                               size_t workspace_bytes, void* stream) {
+  return sp_packed_attention_ex(q, k, v, o, lse, T, Hq, Hkv, d, dtype, cu_seqlens_dev, ndocs, causal,
+                                scale, items_dev, nullptr, n_items, workspace, workspace_bytes, stream);
+}
+
+sp_status sp_packed_attention_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,
+                                 const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal,
+                                 float scale, const sp_item* items_dev, const int32_t* item_heads_dev,
+                                 int64_t n_items, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
   sp_status s = check_shapes(T, Hq, Hkv, d, dtype, ndocs, scale);
   if (s != SP_OK) return s;
   if (n_items < 0 || n_items > 0x7fffffffll) return SP_ERR_INVALID_ARG;
@@ -209,7 +219,7 @@ sp_status sp_packed_attention(const void* q, const void* k, const void* v, void*
   if (!q || !k || !v || !o || !lse || !cu_seqlens_dev || !items_dev || !workspace)
     return SP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(items_dev) ||
-      !aligned16(workspace))
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(item_heads_dev) & 7u) != 0)
     return SP_ERR_INVALID_ARG;
   if (workspace_bytes < sp_packed_attention_workspace_size(n_items)) return SP_ERR_BUFFER_TOO_SMALL;
   unsigned* err;
@@ -217,7 +227,7 @@ sp_status sp_packed_attention(const void* q, const void* k, const void* v, void*
   if (!device_state(&err, &sms)) return SP_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int rpu = dtype == SP_DTYPE_BF16 ? sp::TC_ROWS_PER_UNIT : sp::SIMT_ROWS_PER_UNIT;
-  cudaError_t e = sp::launch_prep(items_dev, n_items, T, Hq, rpu, workspace, err, st);
+  cudaError_t e = sp::launch_prep(items_dev, item_heads_dev, n_items, T, Hq, Hkv, rpu, workspace, err, st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
   AttnArgs a = base_args(q, k, v, o, lse, T, Hq, Hkv, d, cu_seqlens_dev, ndocs, causal, scale, err);
   const sp::WsLayout L = sp::ws_layout(n_items);
@@ -275,7 +285,7 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   if (g > static_cast<long long>(sms) * 16) g = static_cast<long long>(sms) * 16;
   cudaError_t e = sp::launch_bwd_rowdot(o, dout, dvec, T, Hq, d, static_cast<int>(g), st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
-  e = sp::launch_prep(items_dev, n_items, T, Hq, sp::BWD_ROWS_PER_UNIT, workspace, err, st);
+  e = sp::launch_prep(items_dev, nullptr, n_items, T, Hq, Hkv, sp::BWD_ROWS_PER_UNIT, workspace, err, st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
 
   sp::BwdArgs b;

@@ -24,12 +24,23 @@ __device__ long long block_exclusive_scan(long long x, long long* tmp, long long
   return incl - x;
 }
 
-// Groups the items by (rank, Q range) runs, estimates each group's cost
-// (row groups x 128-key tiles), orders groups largest first, and assigns
-// work-unit ranges. One block of 1024 threads. Also validates the items.
+// Groups the items by (rank, Q range, head range) runs, estimates each
+// group's cost (row groups x heads x 128-key tiles), orders groups largest
+// first, and assigns work-unit ranges. One block of 1024 threads. Also
+// validates the items and head ranges.
+__device__ __forceinline__ void item_heads_of(const int32_t* heads, int i, int Hq, int& h0, int& h1) {
+  if (heads) {
+    h0 = heads[2 * i];
+    h1 = heads[2 * i + 1];
+  } else {
+    h0 = 0;
+    h1 = Hq;
+  }
+}
+
 __global__ void __launch_bounds__(1024)
-prep_kernel(const sp_item* __restrict__ items, int n, int T, int Hq, int rpu, int32_t* ws,
-            unsigned* err) {
+prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads, int n, int T, int Hq,
+            int Hkv, int rpu, int32_t* ws, unsigned* err) {
   __shared__ long long scan_tmp[1024];
   __shared__ int bad;
   const WsLayout L = ws_layout(n);
@@ -44,30 +55,36 @@ prep_kernel(const sp_item* __restrict__ items, int n, int T, int Hq, int rpu, in
 
   const int chunk = (n + 1023) / 1024;
   const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
+  const int G = Hq / Hkv;
+  // A new group starts where the rank, Q range or head range changes.
+  auto starts_group = [&](int i) {
+    if (i == 0) return true;
+    const sp_item pv = items[i - 1], it = items[i];
+    int a0, a1, b0, b1;
+    item_heads_of(heads, i - 1, Hq, a0, a1);
+    item_heads_of(heads, i, Hq, b0, b1);
+    return pv.rank != it.rank || pv.q_begin != it.q_begin || pv.q_end != it.q_end || a0 != b0 || a1 != b1;
+  };
   long long cnt = 0;
   for (int i = i0; i < i1; ++i) {
     const sp_item it = items[i];
     if (!(0 <= it.q_begin && it.q_begin < it.q_end && it.q_end <= T && 0 <= it.kv_begin &&
           it.kv_begin <= it.kv_end && it.kv_end <= T))
       bad = 1;
-    bool start = (i == 0);
-    if (!start) {
-      const sp_item pv = items[i - 1];
-      start = pv.rank != it.rank || pv.q_begin != it.q_begin || pv.q_end != it.q_end;
-    }
-    cnt += start;
+    int h0, h1;
+    item_heads_of(heads, i, Hq, h0, h1);
+    const int nh = h1 - h0;
+    // Whole key/value-head groups, or a piece inside one group.
+    const bool whole = nh > 0 && nh % G == 0 && h0 % G == 0;
+    const bool inside = nh > 0 && G % nh == 0 && h0 % nh == 0;
+    if (!(0 <= h0 && h1 <= Hq && (whole || inside))) bad = 1;
+    cnt += starts_group(i);
   }
   long long nseg_ll;
   long long off = block_exclusive_scan(cnt, scan_tmp, &nseg_ll);
   const int nseg = static_cast<int>(nseg_ll);
-  for (int i = i0; i < i1; ++i) {
-    bool start = (i == 0);
-    if (!start) {
-      const sp_item pv = items[i - 1], it = items[i];
-      start = pv.rank != it.rank || pv.q_begin != it.q_begin || pv.q_end != it.q_end;
-    }
-    if (start) starts[off++] = i;
-  }
+  for (int i = i0; i < i1; ++i)
+    if (starts_group(i)) starts[off++] = i;
   if (tid == 0) starts[nseg] = n;
   __syncthreads();
 
@@ -84,9 +101,9 @@ prep_kernel(const sp_item* __restrict__ items, int n, int T, int Hq, int rpu, in
     e.item_hi = hi;
     e.unit_begin = 0;
     e.n_qgroups = qg;
-    e.pad0 = e.pad1 = 0;
+    item_heads_of(heads, lo, Hq, e.h_lo, e.h_hi);
     tmp[s] = e;
-    cost[s] = tiles * qg;
+    cost[s] = tiles * qg * max(e.h_hi - e.h_lo, 0);
   }
   __syncthreads();
 
@@ -106,13 +123,15 @@ prep_kernel(const sp_item* __restrict__ items, int n, int T, int Hq, int rpu, in
   }
   __syncthreads();
 
-  // Q ranges of different groups must not overlap (each output row is
-  // written by exactly one group).
+  // The (Q range x head range) rectangles of different groups must not
+  // overlap (each output row of each head is written by exactly one group).
   if (nseg <= 8192) {
     for (int s = tid; s < nseg; s += 1024) {
-      const int a0 = segs[s].q_lo, a1 = segs[s].q_hi;
+      const int a0 = segs[s].q_lo, a1 = segs[s].q_hi, g0 = segs[s].h_lo, g1 = segs[s].h_hi;
       for (int t2 = s + 1; t2 < nseg; ++t2)
-        if (max(a0, segs[t2].q_lo) < min(a1, segs[t2].q_hi)) bad = 1;
+        if (max(a0, segs[t2].q_lo) < min(a1, segs[t2].q_hi) &&
+            max(g0, segs[t2].h_lo) < min(g1, segs[t2].h_hi))
+          bad = 1;
     }
   }
 
@@ -120,12 +139,12 @@ prep_kernel(const sp_item* __restrict__ items, int n, int T, int Hq, int rpu, in
   const int schunk = (nseg + 1023) / 1024;
   const int s0 = min(nseg, tid * schunk), s1 = min(nseg, s0 + schunk);
   long long units = 0;
-  for (int s = s0; s < s1; ++s) units += static_cast<long long>(segs[s].n_qgroups) * Hq;
+  for (int s = s0; s < s1; ++s) units += static_cast<long long>(segs[s].n_qgroups) * (segs[s].h_hi - segs[s].h_lo);
   long long total;
   long long ub = block_exclusive_scan(units, scan_tmp, &total);
   for (int s = s0; s < s1; ++s) {
     segs[s].unit_begin = static_cast<int32_t>(ub);
-    ub += static_cast<long long>(segs[s].n_qgroups) * Hq;
+    ub += static_cast<long long>(segs[s].n_qgroups) * (segs[s].h_hi - segs[s].h_lo);
   }
   __syncthreads();
   if (tid == 0) {
@@ -192,9 +211,10 @@ __global__ void wait_selftest_kernel(unsigned long long timeout_ns, unsigned* er
 
 }  // namespace
 
-cudaError_t launch_prep(const sp_item* items, int64_t n_items, int32_t T, int32_t Hq,
-                        int32_t rows_per_unit, void* workspace, unsigned* err, cudaStream_t st) {
-  prep_kernel<<<1, 1024, 0, st>>>(items, static_cast<int>(n_items), T, Hq, rows_per_unit,
+cudaError_t launch_prep(const sp_item* items, const int32_t* item_heads, int64_t n_items, int32_t T,
+                        int32_t Hq, int32_t Hkv, int32_t rows_per_unit, void* workspace, unsigned* err,
+                        cudaStream_t st) {
+  prep_kernel<<<1, 1024, 0, st>>>(items, item_heads, static_cast<int>(n_items), T, Hq, Hkv, rows_per_unit,
                                   static_cast<int32_t*>(workspace), err);
   return cudaGetLastError();
 }

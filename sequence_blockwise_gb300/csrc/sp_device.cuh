@@ -39,16 +39,20 @@ __device__ __forceinline__ const SegEntry& seg_of_unit(const AttnArgs& a, int u)
   return a.segs[lo];
 }
 
+// Units of a group: key/value heads slowest, then row groups from the last,
+// then the group's query heads of that key/value head. Gr = query heads of
+// the range per key/value head (G for a range of whole groups).
 __device__ __forceinline__ UnitInfo unit_info(const AttnArgs& a, int u) {
   const SegEntry& s = seg_of_unit(a, u);
   const int local = u - s.unit_begin;
   const int G = a.Hq / a.Hkv;
-  const int per_kv = s.n_qgroups * G;       // units sharing one key/value head
+  const int Gr = min(G, s.h_hi - s.h_lo);
+  const int per_kv = s.n_qgroups * Gr;      // units sharing one key/value head
   const int hk = local / per_kv;
   const int rem = local - hk * per_kv;
-  const int qg = s.n_qgroups - 1 - rem / G;
+  const int qg = s.n_qgroups - 1 - rem / Gr;
   UnitInfo ui;
-  ui.h = hk * G + rem % G;
+  ui.h = s.h_lo + hk * Gr + rem % Gr;
   ui.q0 = s.q_lo + qg * a.rows_per_unit;
   ui.q_lo = s.q_lo;
   ui.q_hi = s.q_hi;

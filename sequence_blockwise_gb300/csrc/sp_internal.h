@@ -13,14 +13,15 @@ namespace sp {
 // Error bits recorded in the per-device error word.
 enum : unsigned { ERR_TIMEOUT_BIT = 1u, ERR_INTERNAL_BIT = 2u };
 
-// One group of items that share a rank and a Q range. After the set-up kernel
-// the table is sorted by estimated cost, largest first.
+// One group of items that share a rank, a Q range and a range of query
+// heads. After the set-up kernel the table is sorted by estimated cost,
+// largest first.
 struct SegEntry {
   int32_t q_lo, q_hi;        // Q rows of the group
   int32_t item_lo, item_hi;  // items [item_lo, item_hi) in schedule order
   int32_t unit_begin;        // first work unit of the group
   int32_t n_qgroups;         // row groups of rows_per_unit rows
-  int32_t pad0, pad1;
+  int32_t h_lo, h_hi;        // query heads [h_lo, h_hi) (all heads unless a head split is given)
 };
 static_assert(sizeof(SegEntry) == 32, "SegEntry is 32 bytes");
 
@@ -70,8 +71,11 @@ struct BwdArgs {
 };
 
 // Launchers (return cudaGetLastError() of the launch).
-cudaError_t launch_prep(const sp_item* items, int64_t n_items, int32_t T, int32_t Hq,
-                        int32_t rows_per_unit, void* workspace, unsigned* err, cudaStream_t st);
+// item_heads: NULL (every item covers all Hq heads) or int32 [n][2] query-head
+// ranges; a range must cover whole key/value-head groups or lie inside one.
+cudaError_t launch_prep(const sp_item* items, const int32_t* item_heads, int64_t n_items, int32_t T,
+                        int32_t Hq, int32_t Hkv, int32_t rows_per_unit, void* workspace, unsigned* err,
+                        cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, const void* tmap_q, const void* tmap_k,
                            const void* tmap_v, int grid, cudaStream_t st);

@@ -505,6 +505,52 @@ sp_status sp_schedule_build_chunked(sp_sched_kind kind, int32_t P, int32_t T, co
   return SP_OK;
 }
 
+sp_status sp_schedule_build_hier(sp_sched_kind inter_kind, int32_t R, int32_t U, int32_t T,
+                                 const int32_t* cu, int32_t ndocs, int32_t causal_i, uint64_t seed,
+                                 int32_t Hq, const int32_t* bounds, sp_item* out, int32_t* out_heads,
+                                 int64_t* inout_n) {
+  if (!inout_n || R < 1 || U < 1 || Hq < 1 || Hq % U != 0 || T < 0) return SP_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(R) * U > (1 << 20)) return SP_ERR_INVALID_ARG;
+  // The Inter-SP schedule over the R groups.
+  int64_t n = 0;
+  sp_status st = sp_schedule_build_chunked(inter_kind, R, T, cu, ndocs, causal_i, seed, bounds, nullptr, &n);
+  if (st != SP_OK) return st;
+  std::vector<sp_item> inter(static_cast<size_t>(n));
+  if (n) {
+    st = sp_schedule_build_chunked(inter_kind, R, T, cu, ndocs, causal_i, seed, bounds, inter.data(), &n);
+    if (st != SP_OK) return st;
+  }
+  const int64_t total = n * U;
+  if (!out) {
+    *inout_n = total;
+    return SP_OK;
+  }
+  if (!out_heads) return SP_ERR_INVALID_ARG;
+  if (*inout_n < total) {
+    *inout_n = total;
+    return SP_ERR_BUFFER_TOO_SMALL;
+  }
+  // Rank g*U + u: group g's items, query heads [u Hq/U, (u+1) Hq/U).
+  const int hs = Hq / U;
+  int64_t w = 0;
+  size_t x = 0;
+  for (int g = 0; g < R; ++g) {
+    const size_t x0 = x;
+    while (x < inter.size() && inter[x].rank == g) ++x;
+    for (int u = 0; u < U; ++u)
+      for (size_t y = x0; y < x; ++y) {
+        sp_item it = inter[y];
+        it.rank = g * U + u;
+        out[w] = it;
+        out_heads[2 * w] = u * hs;
+        out_heads[2 * w + 1] = (u + 1) * hs;
+        ++w;
+      }
+  }
+  *inout_n = w;
+  return SP_OK;
+}
+
 }  // extern "C"
 
 extern "C" sp_status sp_schedule_link_bytes(sp_sched_kind kind, int32_t P, int32_t T,

@@ -1,0 +1,94 @@
+"""Two-level schedules (Inter-SP schedule between R groups, query heads split
+over the U ranks of a group) and the oracle's check for them: the check
+reduces the schedule to U head slices, each an R-rank schedule verified by
+the pinned single-level check with brute-force pair counting, and rejects
+planted defects."""
+import numpy as np
+import pytest
+
+import oracle
+import sequence_blockwise_gb300 as sb
+from sequence_blockwise_gb300 import workloads as wl
+
+
+def _succ(kind, R, seed):
+    return sb.sp_tasp_cycles(R, seed) if kind == sb.SP_SCHED_TASP and R > 1 else None
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("kind,R,U,Hq", [(sb.SP_SCHED_RING, 2, 8, 16), (sb.SP_SCHED_TASP, 3, 2, 8),
+                                         (sb.SP_SCHED_ZIGZAG, 2, 4, 8), (sb.SP_SCHED_TASP, 5, 4, 4),
+                                         (sb.SP_SCHED_RING, 1, 4, 32)])
+def test_hier_schedule_passes_oracle_check(kind, R, U, Hq, causal):
+    T = 720
+    cu = np.array([0, 130, 131, 400, 720], dtype=np.int32)
+    items, heads = sb.sp_schedule_build_hier(kind, R, U, T, cu, causal, Hq, seed=4)
+    flat = sb.sp_schedule_build(kind, R, T, cu, causal, seed=4)
+    assert len(items) == U * len(flat)
+    rc, msg = oracle.check_hier_schedule(kind, R, U, Hq, T, cu, causal, items, heads, _succ(kind, R, 4),
+                                         brute=True)
+    assert rc == 0, msg
+    # Every rank appears, with its own head slice; order by rank.
+    assert np.all(np.diff(items[:, 0]) >= 0)
+    for r in np.unique(items[:, 0]):
+        hs = heads[items[:, 0] == r]
+        u = r % U
+        assert np.all(hs[:, 0] == u * Hq // U) and np.all(hs[:, 1] == (u + 1) * Hq // U)
+
+
+def test_one_rank_per_group_is_the_flat_schedule():
+    w = wl.WORKLOADS[2]
+    cu = wl.cu_seqlens(w)
+    items, heads = sb.sp_schedule_build_hier(w.kind, w.P, 1, w.T, cu, True, w.Hq, seed=w.seed)
+    assert np.array_equal(items, sb.sp_schedule_build(w.kind, w.P, w.T, cu, True, seed=w.seed))
+    assert np.all(heads[:, 0] == 0) and np.all(heads[:, 1] == w.Hq)
+
+
+def test_hier_with_balanced_group_chunks():
+    w = wl.WORKLOADS[2]
+    cu = wl.cu_seqlens(w)
+    R, U = 5, 2
+    bounds = sb.sp_chunk_bounds(sb.SP_CHUNK_BALANCED, R, w.T, cu, True)
+    items, heads = sb.sp_schedule_build_hier(sb.SP_SCHED_TASP, R, U, w.T, cu, True, w.Hq, seed=1,
+                                             bounds=bounds)
+    rc, msg = oracle.check_hier_schedule(sb.SP_SCHED_TASP, R, U, w.Hq, w.T, cu, True, items, heads,
+                                         sb.sp_tasp_cycles(R, 1), bounds=bounds)
+    assert rc == 0, msg
+
+
+def test_hier_check_rejects_planted_defects():
+    T, Hq, R, U = 512, 8, 2, 4
+    cu = np.array([0, 200, 512], dtype=np.int32)
+    items, heads = sb.sp_schedule_build_hier(sb.SP_SCHED_RING, R, U, T, cu, True, Hq)
+    ok = oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, items, heads, brute=True)
+    assert ok[0] == 0, ok[1]
+    # A head range that is not the rank's slice.
+    bad = heads.copy()
+    bad[3] = [0, 2]
+    if not np.array_equal(bad[3], heads[3]):
+        assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, items, bad)[0] == 22
+    # One slice loses an item: its keys are no longer covered.
+    keep = np.ones(len(items), dtype=bool)
+    keep[np.nonzero(items[:, 0] == 1)[0][-1]] = False
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, items[keep], heads[keep])[0] == 39
+    # A duplicated item in one slice: overlap.
+    dup_i = np.concatenate([items, items[-1:]])
+    dup_h = np.concatenate([heads, heads[-1:]])
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, dup_i, dup_h)[0] == 38
+    # A rank outside R * U.
+    big = items.copy()
+    big[0, 0] = R * U
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, big, heads)[0] == 21
+
+
+def test_hier_argument_errors():
+    cu = np.array([0, 256], dtype=np.int32)
+    with pytest.raises(sb.SpError) as e:
+        sb.sp_schedule_build_hier(sb.SP_SCHED_RING, 2, 3, 256, cu, True, 8)  # 8 % 3 != 0
+    assert e.value.code == 1
+    with pytest.raises(sb.SpError) as e:
+        sb.sp_schedule_build_hier(sb.SP_SCHED_TASP, 4, 2, 256, cu, True, 8)  # no decomposition of K4*
+    assert e.value.code == 2
+    with pytest.raises(sb.SpError) as e:
+        sb.sp_schedule_build_hier(sb.SP_SCHED_RING, 0, 2, 256, cu, True, 8)
+    assert e.value.code == 1
