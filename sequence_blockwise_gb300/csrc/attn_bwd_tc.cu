@@ -10,27 +10,28 @@
 // second; TASP abstract: Ring Attention and its decompositions).
 //
 // Three kernels, launched in order on one stream:
-//   bwd_rowdot   D_i per (row, head) into the workspace.
+//   bwd_rowdot   -scale D_i and -LSE_i log2(e) per (row, head) into the workspace.
 //   bwd_dkdv     one unit per (key/value head, 128-key tile), head-major so
 //                that the CTAs running at one time share the Q and dO of one
 //                head group in L2. K and V stay in shared memory while every
-//                64-row Q block that can attend the keys is streamed through
-//                (all query heads of the group). Keys sit on the tensor-memory
-//                lanes: S^T = K Q^T and dP^T = V dO^T (128 x 64 each, double
-//                buffered), the compute warpgroup turns them into P^T and dS^T
-//                (scale folded in) in place, then dV += P^T dO and
-//                dK += dS^T Q read their A operand from tensor memory.
+//                128-row Q tile that can attend the keys streams through (all
+//                query heads of the group). Keys sit on the tensor-memory
+//                lanes: S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
+//                dK += dS^T Q with P^T and dS^T read from tensor memory.
 //   bwd_dq       one unit per (128-row Q tile, query head), walking the same
-//                schedule items as the forward in 64-key steps: S = Q K^T and
-//                dP = dO V^T (128 x 64, double buffered), dS written over S,
-//                dQ += dS K.
-// Double buffering lets the MMA lane issue step n+1's S and dP while step n
-// is being worked on. Each kernel: warp 0 TMA producer, warp 1 TMEM owner and
-// MMA lane, warps 4-7 and 8-11 two compute warpgroups that take alternate
-// steps (step g uses buffer g & 1 and warpgroup g & 1; one TMEM lane, i.e.
-// one key or query row, per thread) and split the epilogue. All tensor maps use {64 dims, 1 head, 64 rows}
+//                schedule items as the forward in 128-key tiles: S = Q K^T,
+//                dP = dO V^T, dQ += dS K with dS read from tensor memory.
+// Every MMA is 128 x 128 x 16 (a 128 x 64 MMA costs as long as a 128 x 128
+// one, so narrower steps would halve the tensor-core rate). Overlap comes from
+// splitting the elementwise work between two compute warpgroups: warpgroup 0
+// turns S into P, warpgroup 1 turns dP into dS, and the MMA lane interleaves
+// (dV or nothing)(g), S(g+1), (dK or dQ)(g), dP(g+1), so that S(g+1) runs
+// while warpgroup 1 works on step g and dP(g+1) while warpgroup 0 works on
+// step g+1. Each kernel: warp 0 TMA producer, warp 1 TMEM owner and MMA lane,
+// warps 4-7 warpgroup 0, warps 8-11 warpgroup 1 (one TMEM lane, i.e. one key
+// or query row, per thread). Tensor maps use {64 dims, 1 head, 64 rows}
 // boxes with 128-byte swizzle; a 128-row tile is two boxes, row r at r x 128
-// bytes of each 64-dim sub-tile, which is the same layout one 128-row box gives.
+// bytes of each 64-dim sub-tile, the layout one 128-row box would give.
 
 #include <cuda.h>
 
@@ -43,59 +44,46 @@ namespace sp {
 namespace {
 
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr int NSTEP = 64;  // rows of the streamed operand per step
 
 template <int D>
 struct BCfg {
-  static constexpr int KSUB = D / 64;                  // 64-dim sub-tiles
-  static constexpr int SUB128 = 128 * 128;             // bytes of a 128-row sub-tile
-  static constexpr int SUB64 = 64 * 128;               // bytes of a 64-row sub-tile
-  static constexpr int TILE128 = KSUB * SUB128;
-  static constexpr int TILE64 = KSUB * SUB64;
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, NSTEP, 0, 0);  // both K-major
-  static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, 0, 1);    // B MN-major
+  static constexpr int KSUB = D / 64;        // 64-dim sub-tiles
+  static constexpr int SUB = 128 * 128;      // bytes of a 128-row sub-tile
+  static constexpr int BOX = 64 * 128;       // bytes of a 64-row box
+  static constexpr int TILE = KSUB * SUB;    // bytes of a 128-row tile
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // both K-major
+  static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, 0, 1);  // B MN-major
   static constexpr int TMEM_COLS = 512;
 };
 
 // K-major operand descriptor (rows = M or N, 64 dims per 128-byte row).
 __device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return smem_desc_sw128(addr, 16, 1024); }
-// MN-major B operand over a tile of 64 rows (K) x D (N): the next 64 columns
-// of N start one 64-row sub-tile further on.
-__device__ __forceinline__ uint64_t desc_mn64(uint32_t addr) { return smem_desc_sw128(addr, 64 * 128, 1024); }
+// MN-major B operand over a 128-row tile: the next 64 columns of N start one
+// sub-tile further on.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr) { return smem_desc_sw128(addr, 128 * 128, 1024); }
 
-// D/16 MMAs contracting over d: C[128 x 64] = A[128 rows] B[64 rows]^T, both
-// K-major; A is a 128-row tile, B a 64-row tile.
+// D/16 MMAs contracting over d: C[128 x 128] = A B^T, A and B 128-row K-major tiles.
 template <int D>
 __device__ __forceinline__ void mma_s(uint32_t d_t, uint32_t a_addr, uint32_t b_addr) {
   using C = BCfg<D>;
   const uint64_t a0 = desc_k(a_addr), b0 = desc_k(b_addr);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint64_t ao = static_cast<uint64_t>(((kk >> 2) * C::SUB128 + (kk & 3) * 32) >> 4);
-    const uint64_t bo = static_cast<uint64_t>(((kk >> 2) * C::SUB64 + (kk & 3) * 32) >> 4);
-    tc_mma_ss(d_t, a0 + ao, b0 + bo, C::IDESC_S, kk > 0 ? 1u : 0u);
+    const uint64_t o = static_cast<uint64_t>(((kk >> 2) * C::SUB + (kk & 3) * 32) >> 4);
+    tc_mma_ss(d_t, a0 + o, b0 + o, C::IDESC_S, kk > 0 ? 1u : 0u);
   }
 }
 
-// 4 MMAs contracting over 64 rows: C[128 x D] (+)= A(tmem, 32 columns of bf16
-// pairs) B(64 rows x D, MN-major).
+// 8 MMAs contracting over 128 rows: C[128 x D] (+)= A(tmem, 64 columns of
+// bf16 pairs) B(128 rows x D, MN-major).
 template <int D>
 __device__ __forceinline__ void mma_acc(uint32_t d_t, uint32_t a_t, uint32_t b_addr, int acc) {
   using C = BCfg<D>;
-  const uint64_t b0 = desc_mn64(b_addr);
+  const uint64_t b0 = desc_mn(b_addr);
 #pragma unroll
-  for (int kk = 0; kk < NSTEP / 16; ++kk)
+  for (int kk = 0; kk < 8; ++kk)
     tc_mma_ts(d_t, a_t + 8 * kk, b0 + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_ACC,
               (acc || kk > 0) ? 1u : 0u);
-}
-
-// TMA of a 64-row block (all D dims) of one head into a 64-row tile.
-template <int D>
-__device__ __forceinline__ void load_rows64(uint32_t dst, const CUtensorMap* m, uint32_t bar, int h,
-                                            int row0) {
-  using C = BCfg<D>;
-#pragma unroll
-  for (int s = 0; s < C::KSUB; ++s) tma_load_3d(dst + s * C::SUB64, m, bar, 64 * s, h, row0);
 }
 
 // TMA of a 128-row block as two 64-row boxes into a 128-row tile (row0 < T).
@@ -109,9 +97,21 @@ __device__ __forceinline__ void load_rows128(uint32_t dst, const CUtensorMap* m,
   const int row1 = row0 + 64 < T ? row0 + 64 : T - 1;
 #pragma unroll
   for (int s = 0; s < C::KSUB; ++s) {
-    tma_load_3d(dst + s * C::SUB128, m, bar, 64 * s, h, row0);
-    tma_load_3d(dst + s * C::SUB128 + C::SUB64, m, bar, 64 * s, h, row1);
+    tma_load_3d(dst + s * C::SUB, m, bar, 64 * s, h, row0);
+    tma_load_3d(dst + s * C::SUB + C::BOX, m, bar, 64 * s, h, row1);
   }
+}
+
+// 4-byte asynchronous copy global -> shared, counted on an mbarrier by
+// cp_async_arrive (no increment of the barrier's expected count).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
 }
 
 // Writes 32 fp32 accumulator columns of one row as bf16.
@@ -131,60 +131,130 @@ __device__ __forceinline__ void store_zero_row_bf16(uint16_t* dst, int n) {
   for (int j = 0; j < n; j += 8) *reinterpret_cast<uint4*>(dst + j) = make_uint4(0, 0, 0, 0);
 }
 
-// Softmax-gradient work of one step for one TMEM lane (one row of the
-// 128-lane operand, 64 columns of the streamed operand): P from S, then dS
-// from P and dP. lse2_of(c) / dd_of(c) give the log2-scaled LSE and D of
-// column c's query (or the row's own when they are per row). Columns outside
-// [lo, hi) get P = dS = 0. P is packed to bf16 pairs into the S columns
-// (32 columns) when keep_p; dS (scale folded in) is packed into dst_ds.
-template <bool kKeepP, typename LseF, typename DF>
-__device__ __forceinline__ void grad_step(uint32_t t_s, uint32_t t_dp, uint32_t dst_ds, int lo, int hi,
-                                          float sl2, float scale, LseF lse2_of, DF dd_of) {
-  uint32_t x[64];
-  {
-    uint32_t a[32];
-    tmem_ld32_sync(t_s, a);
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Loads 64 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t t, uint32_t (&x)[64]) {
+  uint32_t a[32];
+  tmem_ld32_sync(t, a);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) x[c] = a[c];
-    tmem_ld32_sync(t_s + 32, a);
+  for (int c = 0; c < 32; ++c) x[c] = a[c];
+  tmem_ld32_sync(t + 32, a);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) x[32 + c] = a[c];
+  for (int c = 0; c < 32; ++c) x[32 + c] = a[c];
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Per-column values of a step (one per query column, staged in shared memory)
+// or one per-row value broadcast to every column; pair4(c) gives the pairs
+// for columns (c, c+1) and (c+2, c+3).
+struct ColVals {
+  const float* v;
+  __device__ __forceinline__ void pair4(int c, uint64_t& p01, uint64_t& p23) const {
+    const float4 q = *reinterpret_cast<const float4*>(v + c);
+    p01 = f2_pack(q.x, q.y);
+    p23 = f2_pack(q.z, q.w);
   }
+};
+struct RowVal {
+  uint64_t v2;
+  __device__ __forceinline__ void pair4(int, uint64_t& p01, uint64_t& p23) const { p01 = p23 = v2; }
+};
+
+// Warpgroup 0's step: P = 2^(S sl2 + nlse2) (nlse2 = -LSE log2 e) on columns
+// [lo, hi) (0 elsewhere) as bf16 pairs, 64 packed columns written from dst
+// on. In two halves of 64 S columns; half h writes packed columns
+// 32h .. 32h+31 (when dst is S itself, columns half 0 has already read).
+template <bool kMask, typename Src>
+__device__ __forceinline__ void p_from_s_impl(uint32_t t_s, uint32_t dst, int lo, int hi, float sl2, Src nlse2) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-  for (int c = 0; c < 64; ++c) {
-    const float pv = ex2_approx(fmaf(__uint_as_float(x[c]), sl2, -lse2_of(c)));
-    x[c] = __float_as_uint((c >= lo && c < hi) ? pv : 0.f);
-  }
-  if (kKeepP) {
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t x[64];
+    tmem_ld64(t_s + 64 * hh, x);
     uint32_t pk[32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1]));
-    tmem_st32(t_s, pk);
+    for (int c = 0; c < 64; c += 4) {
+      const int c0 = 64 * hh + c;
+      uint64_t n01, n23;
+      nlse2.pair4(c0, n01, n23);
+      const uint64_t a01 = f2_fma(f2_pack(__uint_as_float(x[c]), __uint_as_float(x[c + 1])), sl2x2, n01);
+      const uint64_t a23 = f2_fma(f2_pack(__uint_as_float(x[c + 2]), __uint_as_float(x[c + 3])), sl2x2, n23);
+      float e0, e1, e2, e3;
+      f2_unpack(a01, e0, e1);
+      f2_unpack(a23, e2, e3);
+      float p0 = ex2_approx(e0), p1 = ex2_approx(e1), p2 = ex2_approx(e2), p3 = ex2_approx(e3);
+      if (kMask) {
+        p0 = (c0 >= lo && c0 < hi) ? p0 : 0.f;
+        p1 = (c0 + 1 >= lo && c0 + 1 < hi) ? p1 : 0.f;
+        p2 = (c0 + 2 >= lo && c0 + 2 < hi) ? p2 : 0.f;
+        p3 = (c0 + 3 >= lo && c0 + 3 < hi) ? p3 : 0.f;
+      }
+      pk[c >> 1] = pack_bf16x2(p0, p1);
+      pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+    }
+    tmem_st32(dst + 32 * hh, pk);
   }
+  tmem_wait_st();
+}
+
+// The mask is skipped when no lane of the warp needs it (the tensor-memory
+// accesses must stay warp-uniform).
+template <typename Src>
+__device__ __forceinline__ void p_from_s(uint32_t t_s, uint32_t dst, int lo, int hi, float sl2, Src nlse2) {
+  if (__all_sync(0xffffffffu, lo <= 0 && hi >= 128)) p_from_s_impl<false>(t_s, dst, lo, hi, sl2, nlse2);
+  else p_from_s_impl<true>(t_s, dst, lo, hi, sl2, nlse2);
+}
+
+// Warpgroup 1's step, given P as 64 packed bf16 pairs: dS = P (dP scale +
+// ndsc) with ndsc = -D scale, i.e. P (dP - D) scale, for 128 columns, packed
+// into the first 64 columns of dP (chunk c of 32 dP columns writes packed
+// columns 16c .. 16c+15, already read).
+template <typename Src>
+__device__ __forceinline__ void ds_from_dp(uint32_t t_dp, const uint32_t (&pp)[64], float scale, Src ndsc) {
+  const uint64_t sc2 = f2_pack(scale, scale);
 #pragma unroll
-  for (int ch = 0; ch < 2; ++ch) {
+  for (int ch = 0; ch < 4; ++ch) {
     uint32_t dp[32];
     tmem_ld32_sync(t_dp + 32 * ch, dp);
     uint32_t pk[16];
 #pragma unroll
-    for (int c = 0; c < 32; c += 2) {
+    for (int c = 0; c < 32; c += 4) {
       const int q = 32 * ch + c;
-      const float s0 = __uint_as_float(x[q]) * (__uint_as_float(dp[c]) - dd_of(q)) * scale;
-      const float s1 = __uint_as_float(x[q + 1]) * (__uint_as_float(dp[c + 1]) - dd_of(q + 1)) * scale;
+      uint64_t n01, n23;
+      ndsc.pair4(q, n01, n23);
+      const uint32_t w0 = pp[q >> 1], w1 = pp[(q >> 1) + 1];
+      const uint64_t t01 = f2_fma(f2_pack(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), sc2, n01);
+      const uint64_t t23 = f2_fma(f2_pack(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), sc2, n23);
+      const uint64_t d01 = f2_mul(f2_pack(bf16_lo(w0), bf16_hi(w0)), t01);
+      const uint64_t d23 = f2_mul(f2_pack(bf16_lo(w1), bf16_hi(w1)), t23);
+      float s0, s1, s2, s3;
+      f2_unpack(d01, s0, s1);
+      f2_unpack(d23, s2, s3);
       pk[c >> 1] = pack_bf16x2(s0, s1);
+      pk[(c >> 1) + 1] = pack_bf16x2(s2, s3);
     }
-    tmem_st16(dst_ds + 16 * ch, pk);
+    tmem_st16(t_dp + 16 * ch, pk);
   }
   tmem_wait_st();
 }
 
 // ------------------------------------------------------------------ D_i
 
-// D[h][t] = dO[t][h][:] . O[t][h][:] in fp32 from bf16; one warp per (t, h).
+// ndsc[h][t] = -scale * (dO[t][h][:] . O[t][h][:]) in fp32 from bf16, and
+// nlse2[h][t] = -lse[h][t] * log2(e); one warp per (t, h). The signs and the
+// scale are folded in so that the tensor-core kernels need one FMA per value.
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restrict__ o,
                                                          const uint16_t* __restrict__ dout,
-                                                         float* __restrict__ dvec, int T, int Hq,
-                                                         int d) {
+                                                         const float* __restrict__ lse,
+                                                         float* __restrict__ ndsc, float* __restrict__ nlse2,
+                                                         int T, int Hq, int d, float scale) {
   const int lane = threadIdx.x & 31;
   const long long n = static_cast<long long>(T) * Hq;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
@@ -202,7 +272,11 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restr
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) dvec[static_cast<size_t>(h) * T + t] = acc;
+    if (lane == 0) {
+      const size_t i = static_cast<size_t>(h) * T + t;
+      ndsc[i] = -acc * scale;
+      nlse2[i] = -lse[i] * LOG2E;
+    }
   }
 }
 
@@ -211,25 +285,25 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restr
 template <int D>
 struct KVCfg : BCfg<D> {
   using B = BCfg<D>;
-  static constexpr int QSTAGE = 4;
-  static constexpr int STAGE_BYTES = 2 * B::TILE64 + 1024;  // Q, dO, LSE2[64], D[64]
+  static constexpr int QSTAGE = 2;
+  static constexpr int STAGE_BYTES = 2 * B::TILE + 1024;  // Q, dO, LSE2[128], D[128]
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = B::TILE128;
-  static constexpr int OFF_QD = 2 * B::TILE128;
+  static constexpr int OFF_V = B::TILE;
+  static constexpr int OFF_QD = 2 * B::TILE;
   static constexpr int OFF_BAR = OFF_QD + QSTAGE * STAGE_BYTES;
-  static constexpr int N_BARS = 17;
+  static constexpr int N_BARS = 16;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
 };
 
-enum { KB_KV_FULL = 0, KB_KV_EMPTY = 1, KB_QD_FULL = 2, KB_QD_EMPTY = 6, KB_S_FULL = 10,
-       KB_P_FULL = 12, KB_ACC_FULL = 14, KB_DRAIN = 15, KB_ACC_EMPTY = 16 };
+enum { KB_KV_FULL = 0, KB_KV_EMPTY = 1, KB_QD_FULL = 2, KB_QD_EMPTY = 4, KB_S_FULL = 6, KB_DP_FULL = 7,
+       KB_P_FULL = 8, KB_P_READ = 9, KB_DS_FULL = 10, KB_ACC_FULL = 11, KB_ACC_EMPTY = 12, KB_DRAIN = 13 };
 
 struct KVUnit {
   int k0, k1, hk;  // keys [k0, k1) of key/value head hk
   int qa, qb;      // queries that may attend them
-  int n_steps;     // 64-row Q blocks in [qa, qb) times the heads of the group
+  int n_steps;     // 128-row Q tiles in [qa, qb) times the heads of the group
 };
 
 // Units are head-major: all key tiles of head 0, then head 1, ...
@@ -244,7 +318,7 @@ __device__ __forceinline__ KVUnit kv_unit(const AttnArgs& a, int u) {
   const int d1 = doc_of(a.cu, a.ndocs, w.k1 - 1);
   w.qa = a.causal ? w.k0 : __ldg(a.cu + d0);
   w.qb = __ldg(a.cu + d1 + 1);
-  w.n_steps = ((w.qb - w.qa + NSTEP - 1) / NSTEP) * (a.Hq / a.Hkv);
+  w.n_steps = ((w.qb - w.qa + 127) / 128) * (a.Hq / a.Hkv);
   return w;
 }
 
@@ -271,16 +345,17 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     mbar_init(bar(KB_KV_FULL), 1);
     mbar_init(bar(KB_KV_EMPTY), 1);
     for (int s = 0; s < C::QSTAGE; ++s) {
-      mbar_init(bar(KB_QD_FULL + s), 32);  // every producer lane stores LSE/D; lane 0 arms the bytes
+      mbar_init(bar(KB_QD_FULL + s), 32);  // one asynchronous arrival per producer lane
       mbar_init(bar(KB_QD_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(KB_S_FULL + b), 1);
-      mbar_init(bar(KB_P_FULL + b), 4);
-    }
+    mbar_init(bar(KB_S_FULL), 1);
+    mbar_init(bar(KB_DP_FULL), 1);
+    mbar_init(bar(KB_P_FULL), 4);
+    mbar_init(bar(KB_P_READ), 4);
+    mbar_init(bar(KB_DS_FULL), 4);
     mbar_init(bar(KB_ACC_FULL), 1);
+    mbar_init(bar(KB_ACC_EMPTY), 8);
     mbar_init(bar(KB_DRAIN), 1);
-    mbar_init(bar(KB_ACC_EMPTY), 8);  // every compute warp, after its part of the epilogue
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -299,8 +374,8 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t unit_cnt = 0, gs = 0;
-    int armed_kv = 0, armed_qd[C::QSTAGE] = {0, 0, 0, 0};
-    uint32_t par_kv = 0, par_qd[C::QSTAGE] = {0, 0, 0, 0};
+    int armed_kv = 0, armed_qd[C::QSTAGE] = {0, 0};
+    uint32_t par_kv = 0, par_qd[C::QSTAGE] = {0, 0};
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
       const KVUnit w = kv_unit(f, u);
@@ -308,7 +383,7 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       if (lane == 0) {
         got = mbar_wait_bounded(bar(KB_KV_EMPTY), (unit_cnt & 1) ^ 1, tmo, f.err, abort_flag);
         if (got) {
-          mbar_arrive_expect_tx(bar(KB_KV_FULL), 2 * C::TILE128);
+          mbar_arrive_expect_tx(bar(KB_KV_FULL), 2 * C::TILE);
           armed_kv = 1;
           par_kv = unit_cnt & 1;
           load_rows128<D>(sK, &tmk, bar(KB_KV_FULL), w.hk, w.k0, f.T);
@@ -320,28 +395,27 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         const int st = gs % C::QSTAGE;
         const uint32_t ph = (gs / C::QSTAGE) & 1;
         const int h = w.hk * G + step % G;
-        const int q0 = w.qa + NSTEP * (step / G);
+        const int q0 = w.qa + 128 * (step / G);
         const bool e = mbar_wait_bounded(bar(KB_QD_EMPTY + st), ph ^ 1, tmo, f.err, abort_flag);
         if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-        float* lse2 = reinterpret_cast<float*>(smem + C::OFF_QD + st * C::STAGE_BYTES + 2 * C::TILE64);
-        float* dd = lse2 + NSTEP;
-        for (int idx = lane; idx < NSTEP; idx += 32) {
-          const int row = q0 + idx;
-          const bool in = row < w.qb;
-          lse2[idx] = in ? __ldg(a.lse + static_cast<size_t>(h) * f.T + row) * LOG2E : 0.f;
-          dd[idx] = in ? __ldg(a.dvec + static_cast<size_t>(h) * f.T + row) : 0.f;
-        }
         const uint32_t full = bar(KB_QD_FULL + st);
+        const uint32_t sq = sQD + st * C::STAGE_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(full, 2 * C::TILE64);
-          const uint32_t sq = sQD + st * C::STAGE_BYTES;
-          load_rows64<D>(sq, &tmq, full, h, q0);
-          load_rows64<D>(sq + C::TILE64, &tmdo, full, h, q0);
+          mbar_expect_tx(full, 2 * C::TILE);
+          load_rows128<D>(sq, &tmq, full, h, q0, f.T);
+          load_rows128<D>(sq + C::TILE, &tmdo, full, h, q0, f.T);
           armed_qd[st] = 1;
           par_qd[st] = ph;
-        } else {
-          mbar_arrive(full);
         }
+        // -LSE log2 e and -D scale of the tile's rows (rows past T read row
+        // T-1: masked).
+        const size_t hb = static_cast<size_t>(h) * f.T;
+        for (int idx = lane; idx < 128; idx += 32) {
+          const int row = min(q0 + idx, f.T - 1);
+          cp_async4(sq + 2 * C::TILE + 4 * idx, a.nlse2 + hb + row);
+          cp_async4(sq + 2 * C::TILE + 512 + 4 * idx, a.ndsc + hb + row);
+        }
+        cp_async_arrive(full);
       }
     }
     if (!ok && lane == 0) {
@@ -350,43 +424,59 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       for (int s = 0; s < C::QSTAGE; ++s)
         if (armed_qd[s]) mbar_wait_bounded(bar(KB_QD_FULL + s), par_qd[s], 50000000ull, f.err, &no_abort);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA lane
     if (lane == 0) {
+      const uint32_t tS = tmem + C::TM_S, tdP = tmem + C::TM_DP;
       const uint32_t tdV = tmem + C::TM_DV, tdK = tmem + C::TM_DK;
       uint32_t unit_cnt = 0, gs = 0;
       bool ok = true;
-      // S^T and dP^T of global step g into buffer g & 1.
-      auto issue_s = [&](uint32_t g) -> bool {
-        const int st = g % C::QSTAGE;
-        if (!mbar_wait_bounded(bar(KB_QD_FULL + st), (g / C::QSTAGE) & 1, tmo, f.err, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sq = sQD + st * C::STAGE_BYTES;
-        const uint32_t b = g & 1;
-        mma_s<D>(tmem + C::TM_S + 64 * b, sK, sq);                // S^T = K Q^T
-        mma_s<D>(tmem + C::TM_DP + 64 * b, sV, sq + C::TILE64);   // dP^T = V dO^T
-        tc_commit(bar(KB_S_FULL + b));
-        return true;
-      };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
         const KVUnit w = kv_unit(f, u);
         if (!mbar_wait_bounded(bar(KB_KV_FULL), unit_cnt & 1, tmo, f.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        if (w.n_steps > 0 && !issue_s(gs)) { ok = false; break; }
+        if (w.n_steps > 0) {
+          if (!mbar_wait_bounded(bar(KB_QD_FULL + gs % C::QSTAGE), (gs / C::QSTAGE) & 1, tmo, f.err,
+                                 abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sq = sQD + (gs % C::QSTAGE) * C::STAGE_BYTES;
+          mma_s<D>(tS, sK, sq);              // S^T = K Q^T
+          tc_commit(bar(KB_S_FULL));
+          mma_s<D>(tdP, sV, sq + C::TILE);   // dP^T = V dO^T
+          tc_commit(bar(KB_DP_FULL));
+        }
         // The previous unit's accumulators must have been read out.
         if (unit_cnt > 0 &&
             !mbar_wait_bounded(bar(KB_ACC_EMPTY), (unit_cnt - 1) & 1, tmo, f.err, abort_flag)) { ok = false; break; }
         for (int n = 0; n < w.n_steps; ++n) {
           const uint32_t g = gs + n;
-          if (n + 1 < w.n_steps && !issue_s(g + 1)) { ok = false; break; }
-          const uint32_t b = g & 1;
-          if (!mbar_wait_bounded(bar(KB_P_FULL + b), (g >> 1) & 1, tmo, f.err, abort_flag)) { ok = false; break; }
-          tc_fence_after();
+          const uint32_t ph = g & 1;
+          const bool more = n + 1 < w.n_steps;
           const uint32_t sq = sQD + (g % C::QSTAGE) * C::STAGE_BYTES;
-          mma_acc<D>(tdV, tmem + C::TM_S + 64 * b, sq + C::TILE64, n > 0);  // dV += P^T dO
-          mma_acc<D>(tdK, tmem + C::TM_DP + 64 * b, sq, n > 0);            // dK += dS^T Q
+          const uint32_t sq1 = sQD + ((g + 1) % C::QSTAGE) * C::STAGE_BYTES;
+          if (!mbar_wait_bounded(bar(KB_P_FULL), ph, tmo, f.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_acc<D>(tdV, tS, sq + C::TILE, n > 0);  // dV += P^T dO
+          if (more) {
+            // S(g+1) overwrites P^T(g): dV(g) is issued before it, and
+            // warpgroup 1 has read P^T(g).
+            if (!mbar_wait_bounded(bar(KB_P_READ), ph, tmo, f.err, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_bounded(bar(KB_QD_FULL + (g + 1) % C::QSTAGE), ((g + 1) / C::QSTAGE) & 1, tmo,
+                                   f.err, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            mma_s<D>(tS, sK, sq1);
+            tc_commit(bar(KB_S_FULL));
+          }
+          if (!mbar_wait_bounded(bar(KB_DS_FULL), ph, tmo, f.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_acc<D>(tdK, tdP, sq, n > 0);  // dK += dS^T Q
           tc_commit(bar(KB_QD_EMPTY + g % C::QSTAGE));
+          if (more) {
+            mma_s<D>(tdP, sV, sq1 + C::TILE);
+            tc_commit(bar(KB_DP_FULL));
+          }
         }
         if (!ok) break;
         gs += w.n_steps;
@@ -400,10 +490,11 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute
-    const int wg = (warp - 4) >> 2;  // warpgroup: takes the steps g with g & 1 == wg
+    const int wg = (warp - 4) >> 2;  // 0: S -> P, 1: dP -> dS
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::TM_S, tdP = tmem + lane_off + C::TM_DP;
     const uint32_t tAcc = tmem + lane_off + (wg == 0 ? C::TM_DV : C::TM_DK);
     uint16_t* const out = static_cast<uint16_t*>(wg == 0 ? a.dv : a.dk);
     const float sl2 = f.scale_log2, scale = f.scale;
@@ -421,25 +512,39 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       }
       for (int n = 0; n < w.n_steps; ++n) {
         const uint32_t g = gs + n;
-        const uint32_t b = g & 1;
-        if (static_cast<int>(b) != wg) continue;
-        const int st = g % C::QSTAGE;
-        const int q0 = w.qa + NSTEP * (n / G);
-        bool e = mbar_wait_bounded(bar(KB_S_FULL + b), (g >> 1) & 1, tmo, f.err, abort_flag);
-        e = e && mbar_wait_bounded(bar(KB_QD_FULL + st), (g / C::QSTAGE) & 1, tmo, f.err, abort_flag);
-        if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-        tc_fence_after();
-        const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_QD + st * C::STAGE_BYTES + 2 * C::TILE64);
-        const float* dd = lse2 + NSTEP;
-        const int clo = kvalid ? max(lo, q0) - q0 : 0;
-        const int chi = kvalid ? min(hi, q0 + NSTEP) - q0 : 0;
-        const uint32_t tS = tmem + lane_off + C::TM_S + 64 * b;
-        const uint32_t tdP = tmem + lane_off + C::TM_DP + 64 * b;
-        grad_step<true>(tS, tdP, tdP, clo, chi, sl2, scale, [&](int c) { return lse2[c]; },
-                        [&](int c) { return dd[c]; });
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KB_P_FULL + b));
+        const uint32_t ph = g & 1;
+        const int q0 = w.qa + 128 * (n / G);
+        const uint8_t* stage = smem + C::OFF_QD + (g % C::QSTAGE) * C::STAGE_BYTES + 2 * C::TILE;
+        const uint32_t qd_bar = bar(KB_QD_FULL + g % C::QSTAGE), qd_ph = (g / C::QSTAGE) & 1;
+        if (wg == 0) {
+          bool e = mbar_wait_bounded(bar(KB_S_FULL), ph, tmo, f.err, abort_flag);
+          e = e && mbar_wait_bounded(qd_bar, qd_ph, tmo, f.err, abort_flag);
+          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+          tc_fence_after();
+          const int clo = kvalid ? max(lo, q0) - q0 : 0;
+          const int chi = kvalid ? min(hi, q0 + 128) - q0 : 0;
+          p_from_s(tS, tS, clo, chi, sl2, ColVals{reinterpret_cast<const float*>(stage)});
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(KB_P_FULL));
+        } else {
+          bool e = mbar_wait_bounded(bar(KB_P_FULL), ph, tmo, f.err, abort_flag);
+          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t pp[64];
+          tmem_ld64(tS, pp);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(KB_P_READ));
+          e = mbar_wait_bounded(bar(KB_DP_FULL), ph, tmo, f.err, abort_flag);
+          e = e && mbar_wait_bounded(qd_bar, qd_ph, tmo, f.err, abort_flag);
+          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+          tc_fence_after();
+          ds_from_dp(tdP, pp, scale, ColVals{reinterpret_cast<const float*>(stage + 512)});
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(KB_DS_FULL));
+        }
       }
       if (!ok) break;
       gs += w.n_steps;
@@ -476,45 +581,19 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
 template <int D>
 struct QCfg : BCfg<D> {
   using B = BCfg<D>;
-  static constexpr int KSTAGE = 4;
+  static constexpr int KSTAGE = 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = B::TILE128;
-  static constexpr int OFF_KV = 2 * B::TILE128;  // stage s: K at +0, V at +TILE64
-  static constexpr int OFF_BAR = OFF_KV + KSTAGE * 2 * B::TILE64;
-  static constexpr int N_BARS = 17;
+  static constexpr int OFF_DO = B::TILE;
+  static constexpr int OFF_KV = 2 * B::TILE;  // stage s: K at +0, V at +TILE
+  static constexpr int OFF_BAR = OFF_KV + KSTAGE * 2 * B::TILE;
+  static constexpr int N_BARS = 16;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
-  static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;
+  static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_STASH = 384;  // stash: P as 64 bf16-pair columns
 };
 
-enum { QB_Q_FULL = 0, QB_Q_EMPTY = 1, QB_KV_FULL = 2, QB_KV_EMPTY = 6, QB_S_FULL = 10, QB_P_FULL = 12,
-       QB_ACC_FULL = 14, QB_DRAIN = 15, QB_ACC_EMPTY = 16 };
-
-// Key steps of 64 over a unit's items for one Q tile: the forward's cursor
-// (item key ranges clipped to the keys the tile's rows may attend) walked in
-// 64-key blocks. full = every (row, key) of the block is valid.
-__device__ __forceinline__ bool next_block64(const AttnArgs& a, Cursor& c, const QTile& qt, int& ka,
-                                             int& kb, bool& full) {
-  while (true) {
-    if (c.k0 >= c.kv_e) {
-      if (c.item >= c.item_end) return false;
-      int b, e;
-      item_range(a, c.item, b, e);
-      ++c.item;
-      c.k0 = max(b, c.lo);
-      c.kv_e = min(e, c.hi);
-      continue;
-    }
-    ka = c.k0;
-    kb = min(c.k0 + NSTEP, c.kv_e);
-    c.k0 += NSTEP;
-    if (a.causal && ka > qt.qb - 1) continue;
-    if (qt.de <= ka || kb <= qt.ds) continue;
-    full = qt.qb - qt.qa == 128 && kb - ka == NSTEP && qt.one_doc && ka >= qt.ds && kb <= qt.de &&
-           (!a.causal || kb - 1 <= qt.qa);
-    return true;
-  }
-}
+enum { QB_Q_FULL = 0, QB_Q_EMPTY = 1, QB_KV_FULL = 2, QB_KV_EMPTY = 4, QB_S_FULL = 6, QB_DP_FULL = 7,
+       QB_P_FULL = 8, QB_P_READ = 9, QB_DS_FULL = 10, QB_ACC_FULL = 11, QB_ACC_EMPTY = 12, QB_DRAIN = 13 };
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -541,13 +620,14 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       mbar_init(bar(QB_KV_FULL + s), 1);
       mbar_init(bar(QB_KV_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(QB_S_FULL + b), 1);
-      mbar_init(bar(QB_P_FULL + b), 4);
-    }
+    mbar_init(bar(QB_S_FULL), 1);
+    mbar_init(bar(QB_DP_FULL), 1);
+    mbar_init(bar(QB_P_FULL), 4);
+    mbar_init(bar(QB_P_READ), 4);
+    mbar_init(bar(QB_DS_FULL), 4);
     mbar_init(bar(QB_ACC_FULL), 1);
-    mbar_init(bar(QB_DRAIN), 1);
     mbar_init(bar(QB_ACC_EMPTY), 8);
+    mbar_init(bar(QB_DRAIN), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -564,37 +644,42 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   const int G = f.Hq / f.Hkv;
   const unsigned long long tmo = f.timeout_ns;
 
+  // The unit's single Q tile; the second slot of the shared tile walk stays empty.
+  auto unit_tiles = [&](const UnitInfo& ui, QTile (&qt)[2]) {
+    qt[0] = make_qtile(f, ui, 0);
+    qt[1].qa = qt[1].qb = qt[1].ds = qt[1].de = qt[1].one_doc = 0;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t kv_cnt = 0, unit_cnt = 0;
-      int armed_q = 0, armed_kv[C::KSTAGE] = {0, 0, 0, 0};
-      uint32_t par_q = 0, par_kv[C::KSTAGE] = {0, 0, 0, 0};
+      int armed_q = 0, armed_kv[C::KSTAGE] = {0, 0};
+      uint32_t par_q = 0, par_kv[C::KSTAGE] = {0, 0};
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
         const UnitInfo ui = unit_info(f, u);
-        const QTile qt = make_qtile(f, ui, 0);
-        const QTile qts[2] = {qt, QTile{0, 0, 0, 0, 0}};
+        QTile qt[2];
+        unit_tiles(ui, qt);
         const int hk = ui.h / G;
         if (!mbar_wait_bounded(bar(QB_Q_EMPTY), (unit_cnt & 1) ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(QB_Q_FULL), 2 * C::TILE128);
+        mbar_arrive_expect_tx(bar(QB_Q_FULL), 2 * C::TILE);
         armed_q = 1;
         par_q = unit_cnt & 1;
         load_rows128<D>(sQ, &tmq, bar(QB_Q_FULL), ui.h, ui.q0, f.T);
         load_rows128<D>(sDO, &tmdo, bar(QB_Q_FULL), ui.h, ui.q0, f.T);
-        Cursor cur = make_cursor(ui, qts, f.causal);
-        int ka, kb;
-        bool full;
-        while (next_block64(f, cur, qt, ka, kb, full)) {
+        Cursor cur = make_cursor(ui, qt, f.causal);
+        int ka, kb, cls[2];
+        while (next_tile(f, cur, qt, ka, kb, cls)) {
           const int st = kv_cnt % C::KSTAGE;
           const uint32_t ph = (kv_cnt / C::KSTAGE) & 1;
           if (!mbar_wait_bounded(bar(QB_KV_EMPTY + st), ph ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(QB_KV_FULL + st), 2 * C::TILE64);
+          mbar_arrive_expect_tx(bar(QB_KV_FULL + st), 2 * C::TILE);
           armed_kv[st] = 1;
           par_kv[st] = ph;
-          const uint32_t skv = sKV + st * 2 * C::TILE64;
-          load_rows64<D>(skv, &tmk, bar(QB_KV_FULL + st), hk, ka);
-          load_rows64<D>(skv + C::TILE64, &tmv, bar(QB_KV_FULL + st), hk, ka);
+          const uint32_t skv = sKV + st * 2 * C::TILE;
+          load_rows128<D>(skv, &tmk, bar(QB_KV_FULL + st), hk, ka, f.T);
+          load_rows128<D>(skv + C::TILE, &tmv, bar(QB_KV_FULL + st), hk, ka, f.T);
           ++kv_cnt;
         }
       }
@@ -609,46 +694,59 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA lane
     if (lane == 0) {
-      const uint32_t tdQ = tmem + C::TM_DQ;
+      const uint32_t tS = tmem + C::TM_S, tdP = tmem + C::TM_DP, tdQ = tmem + C::TM_DQ;
       uint32_t kv_cnt = 0, unit_cnt = 0;
       bool ok = true;
-      // S and dP of key block g into buffer g & 1.
-      auto issue_s = [&](uint32_t g) -> bool {
-        const int st = g % C::KSTAGE;
-        if (!mbar_wait_bounded(bar(QB_KV_FULL + st), (g / C::KSTAGE) & 1, tmo, f.err, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t skv = sKV + st * 2 * C::TILE64;
-        const uint32_t b = g & 1;
-        mma_s<D>(tmem + C::TM_S + 64 * b, sQ, skv);                // S = Q K^T
-        mma_s<D>(tmem + C::TM_DP + 64 * b, sDO, skv + C::TILE64);  // dP = dO V^T
-        tc_commit(bar(QB_S_FULL + b));
-        return true;
-      };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
         const UnitInfo ui = unit_info(f, u);
-        const QTile qt = make_qtile(f, ui, 0);
-        const QTile qts[2] = {qt, QTile{0, 0, 0, 0, 0}};
+        QTile qt[2];
+        unit_tiles(ui, qt);
         if (!mbar_wait_bounded(bar(QB_Q_FULL), unit_cnt & 1, tmo, f.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // Count the unit's key blocks (the walk is cheap and identical in every role).
         int nblk = 0;
         {
-          Cursor cur = make_cursor(ui, qts, f.causal);
-          int ka, kb;
-          bool full;
-          while (next_block64(f, cur, qt, ka, kb, full)) ++nblk;
+          Cursor cur = make_cursor(ui, qt, f.causal);
+          int ka, kb, cls[2];
+          while (next_tile(f, cur, qt, ka, kb, cls)) ++nblk;
         }
-        if (nblk > 0 && !issue_s(kv_cnt)) { ok = false; break; }
+        if (nblk > 0) {
+          const uint32_t g = kv_cnt;
+          if (!mbar_wait_bounded(bar(QB_KV_FULL + g % C::KSTAGE), (g / C::KSTAGE) & 1, tmo, f.err,
+                                 abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t skv = sKV + (g % C::KSTAGE) * 2 * C::TILE;
+          mma_s<D>(tS, sQ, skv);               // S = Q K^T
+          tc_commit(bar(QB_S_FULL));
+          mma_s<D>(tdP, sDO, skv + C::TILE);   // dP = dO V^T
+          tc_commit(bar(QB_DP_FULL));
+        }
         if (unit_cnt > 0 &&
             !mbar_wait_bounded(bar(QB_ACC_EMPTY), (unit_cnt - 1) & 1, tmo, f.err, abort_flag)) { ok = false; break; }
         for (int n = 0; n < nblk; ++n) {
           const uint32_t g = kv_cnt + n;
-          if (n + 1 < nblk && !issue_s(g + 1)) { ok = false; break; }
-          const uint32_t b = g & 1;
-          if (!mbar_wait_bounded(bar(QB_P_FULL + b), (g >> 1) & 1, tmo, f.err, abort_flag)) { ok = false; break; }
+          const uint32_t ph = g & 1;
+          const bool more = n + 1 < nblk;
+          const uint32_t skv = sKV + (g % C::KSTAGE) * 2 * C::TILE;
+          const uint32_t skv1 = sKV + ((g + 1) % C::KSTAGE) * 2 * C::TILE;
+          if (more) {
+            // Warpgroup 1 has read the stashed P(g) (so warpgroup 0, which
+            // starts on S(g+1), may overwrite the stash), and S(g) was read
+            // before P(g) was stashed: S may be overwritten.
+            if (!mbar_wait_bounded(bar(QB_P_READ), ph, tmo, f.err, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_bounded(bar(QB_KV_FULL + (g + 1) % C::KSTAGE), ((g + 1) / C::KSTAGE) & 1, tmo,
+                                   f.err, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            mma_s<D>(tS, sQ, skv1);
+            tc_commit(bar(QB_S_FULL));
+          }
+          if (!mbar_wait_bounded(bar(QB_DS_FULL), ph, tmo, f.err, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          mma_acc<D>(tdQ, tmem + C::TM_S + 64 * b, sKV + (g % C::KSTAGE) * 2 * C::TILE64, n > 0);  // dQ += dS K
+          mma_acc<D>(tdQ, tdP, skv, n > 0);  // dQ += dS K
           tc_commit(bar(QB_KV_EMPTY + g % C::KSTAGE));
+          if (more) {
+            mma_s<D>(tdP, sDO, skv1 + C::TILE);
+            tc_commit(bar(QB_DP_FULL));
+          }
         }
         if (!ok) break;
         kv_cnt += nblk;
@@ -662,56 +760,68 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute
-    const int wg = (warp - 4) >> 2;  // warpgroup: takes the blocks g with g & 1 == wg
+    const int wg = (warp - 4) >> 2;  // 0: S -> P, 1: dP -> dS
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::TM_S, tdP = tmem + lane_off + C::TM_DP;
     const uint32_t tdQ = tmem + lane_off + C::TM_DQ;
     const float sl2 = f.scale_log2, scale = f.scale;
     uint32_t unit_cnt = 0, g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
       const UnitInfo ui = unit_info(f, u);
-      const QTile qt = make_qtile(f, ui, 0);
-      const QTile qts[2] = {qt, QTile{0, 0, 0, 0, 0}};
+      QTile qt[2];
+      unit_tiles(ui, qt);
       const int t = ui.q0 + r;
-      const bool valid = t >= qt.qa && t < qt.qb;
+      const bool valid = t >= qt[0].qa && t < qt[0].qb;
       int rds = 0, rde = 0;
-      float lse2 = 0.f, di = 0.f;
+      float nlse2 = 0.f, ndsc = 0.f;
       if (valid) {
         const int dd = doc_of(f.cu, f.ndocs, t);
         rds = __ldg(f.cu + dd);
         rde = __ldg(f.cu + dd + 1);
-        lse2 = __ldg(a.lse + static_cast<size_t>(ui.h) * f.T + t) * LOG2E;
-        di = __ldg(a.dvec + static_cast<size_t>(ui.h) * f.T + t);
+        nlse2 = __ldg(a.nlse2 + static_cast<size_t>(ui.h) * f.T + t);
+        ndsc = __ldg(a.ndsc + static_cast<size_t>(ui.h) * f.T + t);
       }
       const int rend = f.causal ? min(rde, t + 1) : rde;
       int nblk = 0;
-      Cursor cur = make_cursor(ui, qts, f.causal);
-      int ka, kb;
-      bool full;
-      while (next_block64(f, cur, qt, ka, kb, full)) {
-        const uint32_t b = g & 1;
-        if (static_cast<int>(b) != wg) {
-          ++g;
-          ++nblk;
-          continue;
+      Cursor cur = make_cursor(ui, qt, f.causal);
+      int ka, kb, cls[2];
+      while (next_tile(f, cur, qt, ka, kb, cls)) {
+        const uint32_t ph = g & 1;
+        const uint32_t stash = tmem + lane_off + C::TM_STASH;
+        if (wg == 0) {
+          // S(g) is issued only after warpgroup 1 read the stash of block g-1.
+          bool e = mbar_wait_bounded(bar(QB_S_FULL), ph, tmo, f.err, abort_flag);
+          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+          tc_fence_after();
+          int lo = 0, hi = 128;
+          if (cls[0] != CLS_FULL) {
+            lo = valid ? max(ka, rds) - ka : 0;
+            hi = valid ? min(kb, rend) - ka : 0;
+          }
+          p_from_s(tS, stash, lo, hi, sl2, RowVal{f2_pack(nlse2, nlse2)});
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(QB_P_FULL));
+        } else {
+          bool e = mbar_wait_bounded(bar(QB_P_FULL), ph, tmo, f.err, abort_flag);
+          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t pp[64];
+          tmem_ld64(stash, pp);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(QB_P_READ));
+          e = mbar_wait_bounded(bar(QB_DP_FULL), ph, tmo, f.err, abort_flag);
+          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+          tc_fence_after();
+          ds_from_dp(tdP, pp, scale, RowVal{f2_pack(ndsc, ndsc)});
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(QB_DS_FULL));
         }
-        const bool e = mbar_wait_bounded(bar(QB_S_FULL + b), (g >> 1) & 1, tmo, f.err, abort_flag);
-        if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-        tc_fence_after();
-        int lo = 0, hi = NSTEP;
-        if (!full) {
-          lo = valid ? max(ka, rds) - ka : 0;
-          hi = valid ? min(kb, rend) - ka : 0;
-        }
-        const uint32_t tS = tmem + lane_off + C::TM_S + 64 * b;
-        const uint32_t tdP = tmem + lane_off + C::TM_DP + 64 * b;
-        grad_step<false>(tS, tdP, tS, lo, hi, sl2, scale, [&](int) { return lse2; },
-                         [&](int) { return di; });
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(QB_P_FULL + b));
         ++g;
         ++nblk;
       }
@@ -754,10 +864,10 @@ cudaError_t launch_cfg(K kern, int grid, cudaStream_t st, const BwdArgs& a, cons
 
 }  // namespace
 
-cudaError_t launch_bwd_rowdot(const void* o, const void* dout, float* dvec, int T, int Hq, int d,
-                              int grid, cudaStream_t st) {
-  bwd_rowdot_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(o),
-                                         static_cast<const uint16_t*>(dout), dvec, T, Hq, d);
+cudaError_t launch_bwd_rowdot(const void* o, const void* dout, const float* lse, float* ndsc, float* nlse2,
+                              int T, int Hq, int d, float scale, int grid, cudaStream_t st) {
+  bwd_rowdot_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                                         lse, ndsc, nlse2, T, Hq, d, scale);
   return cudaGetLastError();
 }
 

@@ -246,8 +246,9 @@ size_t sp_packed_attention_backward_workspace_size(int64_t n_items, int32_t T, i
   if (n_items < 0) n_items = 0;
   if (T < 0) T = 0;
   if (Hq < 0) Hq = 0;
+  // D and LSE * log2(e) per (head, row).
   const size_t rowdot = (static_cast<size_t>(T) * Hq * sizeof(float) + 255) & ~static_cast<size_t>(255);
-  return sp::ws_layout(n_items).total + rowdot;
+  return sp::ws_layout(n_items).total + 2 * rowdot;
 }
 
 sp_status sp_packed_attention_backward(const void* q, const void* k, const void* v, const void* o,
@@ -279,11 +280,14 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const sp::WsLayout L = sp::ws_layout(n_items);
   float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.total);
+  float* lse2 = reinterpret_cast<float*>(
+      static_cast<char*>(workspace) + L.total +
+      ((static_cast<size_t>(T) * Hq * sizeof(float) + 255) & ~static_cast<size_t>(255)));
 
   const long long warps = static_cast<long long>(T) * Hq;
   long long g = (warps + 7) / 8;
   if (g > static_cast<long long>(sms) * 16) g = static_cast<long long>(sms) * 16;
-  cudaError_t e = sp::launch_bwd_rowdot(o, dout, dvec, T, Hq, d, static_cast<int>(g), st);
+  cudaError_t e = sp::launch_bwd_rowdot(o, dout, lse, dvec, lse2, T, Hq, d, scale, static_cast<int>(g), st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
   e = sp::launch_prep(items_dev, nullptr, n_items, T, Hq, Hkv, sp::BWD_ROWS_PER_UNIT, workspace, err, st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
@@ -296,7 +300,8 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   b.fwd.segs = reinterpret_cast<const sp::SegEntry*>(static_cast<const char*>(workspace) + L.off_segs);
   b.fwd.rows_per_unit = sp::BWD_ROWS_PER_UNIT;
   b.lse = lse;
-  b.dvec = dvec;
+  b.ndsc = dvec;
+  b.nlse2 = lse2;
   b.dq = dq;
   b.dk = dk;
   b.dv = dv;

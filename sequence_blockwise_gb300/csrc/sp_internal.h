@@ -63,8 +63,9 @@ struct AttnArgs {
 // and schedule tables (its o and lse fields are unused).
 struct BwdArgs {
   AttnArgs fwd;
-  const float* lse;   // [Hq][T] natural-log LSE written by the forward
-  const float* dvec;  // [Hq][T] D_i = dO_i . O_i
+  const float* lse;    // [Hq][T] natural-log LSE written by the forward
+  const float* ndsc;   // [Hq][T] -scale * D_i, D_i = dO_i . O_i
+  const float* nlse2;  // [Hq][T] -LSE_i * log2(e)
   void* dq;           // bf16 [T][Hq][d]
   void* dk;           // bf16 [T][Hkv][d]
   void* dv;           // bf16 [T][Hkv][d]
@@ -81,8 +82,8 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const void* tmap_q, const void* tm
                            const void* tmap_v, int grid, cudaStream_t st);
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
                              int32_t rows, int32_t Hq, int32_t d, int grid, cudaStream_t st);
-cudaError_t launch_bwd_rowdot(const void* o, const void* dout, float* dvec, int T, int Hq, int d,
-                              int grid, cudaStream_t st);
+cudaError_t launch_bwd_rowdot(const void* o, const void* dout, const float* lse, float* ndsc, float* nlse2,
+                              int T, int Hq, int d, float scale, int grid, cudaStream_t st);
 // dQ kernel (walks the schedule in fwd) then the dK/dV kernel, both bf16.
 cudaError_t launch_bwd_tc(const BwdArgs& a, const void* tmap_q, const void* tmap_k,
                           const void* tmap_v, const void* tmap_do, int grid, cudaStream_t st);
