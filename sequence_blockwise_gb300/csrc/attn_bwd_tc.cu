@@ -22,14 +22,14 @@
 //                schedule items as the forward in 128-key tiles: S = Q K^T,
 //                dP = dO V^T, dQ += dS K with dS read from tensor memory.
 // Every MMA is 128 x 128 x 16 (a 128 x 64 MMA costs as long as a 128 x 128
-// one, so narrower steps would halve the tensor-core rate). Overlap comes from
-// splitting the elementwise work between two compute warpgroups: warpgroup 0
-// turns S into P, warpgroup 1 turns dP into dS, and the MMA lane interleaves
-// (dV or nothing)(g), S(g+1), (dK or dQ)(g), dP(g+1), so that S(g+1) runs
-// while warpgroup 1 works on step g and dP(g+1) while warpgroup 0 works on
-// step g+1. Each kernel: warp 0 TMA producer, warp 1 TMEM owner and MMA lane,
-// warps 4-7 warpgroup 0, warps 8-11 warpgroup 1 (one TMEM lane, i.e. one key
-// or query row, per thread). Tensor maps use {64 dims, 1 head, 64 rows}
+// one, so narrower steps would halve the tensor-core rate). The elementwise
+// work of a step is split by columns between two compute warpgroups (64
+// columns each, P kept in registers between the S and the dP phase), and the
+// MMA lane interleaves (dV or nothing)(g), S(g+1), (dK or dQ)(g), dP(g+1):
+// S(g+1) runs while the warpgroups turn dP(g) into dS(g), and dK/dQ(g) and
+// dP(g+1) run while they turn S(g+1) into P. Each kernel: warp 0 TMA
+// producer, warp 1 TMEM owner and MMA lane, warps 4-11 two compute
+// warpgroups (one TMEM lane, i.e. one key or query row, per thread). Tensor maps use {64 dims, 1 head, 64 rows}
 // boxes with 128-byte swizzle; a 128-row tile is two boxes, row r at r x 128
 // bytes of each 64-dim sub-tile, the layout one 128-row box would give.
 
@@ -74,16 +74,19 @@ __device__ __forceinline__ void mma_s(uint32_t d_t, uint32_t a_addr, uint32_t b_
   }
 }
 
-// 8 MMAs contracting over 128 rows: C[128 x D] (+)= A(tmem, 64 columns of
-// bf16 pairs) B(128 rows x D, MN-major).
+// 8 MMAs contracting over 128 rows: C[128 x D] (+)= A(tmem) B(128 rows x D,
+// MN-major). A holds bf16 pairs in two 32-column halves of a 128-column
+// region: rows 0-63 of the contraction in columns 0-31, rows 64-127 in
+// columns 64-95 (each written by one compute warpgroup over the columns it
+// read).
 template <int D>
 __device__ __forceinline__ void mma_acc(uint32_t d_t, uint32_t a_t, uint32_t b_addr, int acc) {
   using C = BCfg<D>;
   const uint64_t b0 = desc_mn(b_addr);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    tc_mma_ts(d_t, a_t + 8 * kk, b0 + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_ACC,
-              (acc || kk > 0) ? 1u : 0u);
+    tc_mma_ts(d_t, a_t + 8 * kk + (kk >= 4 ? 32 : 0), b0 + static_cast<uint64_t>(kk * (2048 >> 4)),
+              C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
 }
 
 // TMA of a 128-row block as two 64-row boxes into a 128-row tile (row0 < T).
@@ -167,82 +170,82 @@ struct RowVal {
   __device__ __forceinline__ void pair4(int, uint64_t& p01, uint64_t& p23) const { p01 = p23 = v2; }
 };
 
-// Warpgroup 0's step: P = 2^(S sl2 + nlse2) (nlse2 = -LSE log2 e) on columns
-// [lo, hi) (0 elsewhere) as bf16 pairs, 64 packed columns written from dst
-// on. In two halves of 64 S columns; half h writes packed columns
-// 32h .. 32h+31 (when dst is S itself, columns half 0 has already read).
+// One compute warpgroup's half of a step (64 of the 128 columns, starting
+// at column c0 of the operand): given S of those columns in p[], replaces it
+// by P = 2^(S sl2 + nlse2) with nlse2 = -LSE log2 e on columns [lo, hi) (0
+// elsewhere), in fp32.
 template <bool kMask, typename Src>
-__device__ __forceinline__ void p_from_s_impl(uint32_t t_s, uint32_t dst, int lo, int hi, float sl2, Src nlse2) {
+__device__ __forceinline__ void p_half_impl(int c0, int lo, int hi, float sl2, Src nlse2, uint32_t (&p)[64]) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    uint32_t x[64];
-    tmem_ld64(t_s + 64 * hh, x);
-    uint32_t pk[32];
-#pragma unroll
-    for (int c = 0; c < 64; c += 4) {
-      const int c0 = 64 * hh + c;
-      uint64_t n01, n23;
-      nlse2.pair4(c0, n01, n23);
-      const uint64_t a01 = f2_fma(f2_pack(__uint_as_float(x[c]), __uint_as_float(x[c + 1])), sl2x2, n01);
-      const uint64_t a23 = f2_fma(f2_pack(__uint_as_float(x[c + 2]), __uint_as_float(x[c + 3])), sl2x2, n23);
-      float e0, e1, e2, e3;
-      f2_unpack(a01, e0, e1);
-      f2_unpack(a23, e2, e3);
-      float p0 = ex2_approx(e0), p1 = ex2_approx(e1), p2 = ex2_approx(e2), p3 = ex2_approx(e3);
-      if (kMask) {
-        p0 = (c0 >= lo && c0 < hi) ? p0 : 0.f;
-        p1 = (c0 + 1 >= lo && c0 + 1 < hi) ? p1 : 0.f;
-        p2 = (c0 + 2 >= lo && c0 + 2 < hi) ? p2 : 0.f;
-        p3 = (c0 + 3 >= lo && c0 + 3 < hi) ? p3 : 0.f;
-      }
-      pk[c >> 1] = pack_bf16x2(p0, p1);
-      pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+  for (int c = 0; c < 64; c += 4) {
+    const int cc = c0 + c;
+    uint64_t n01, n23;
+    nlse2.pair4(cc, n01, n23);
+    const uint64_t a01 = f2_fma(f2_pack(__uint_as_float(p[c]), __uint_as_float(p[c + 1])), sl2x2, n01);
+    const uint64_t a23 = f2_fma(f2_pack(__uint_as_float(p[c + 2]), __uint_as_float(p[c + 3])), sl2x2, n23);
+    float e0, e1, e2, e3;
+    f2_unpack(a01, e0, e1);
+    f2_unpack(a23, e2, e3);
+    float p0 = ex2_approx(e0), p1 = ex2_approx(e1), p2 = ex2_approx(e2), p3 = ex2_approx(e3);
+    if (kMask) {
+      p0 = (cc >= lo && cc < hi) ? p0 : 0.f;
+      p1 = (cc + 1 >= lo && cc + 1 < hi) ? p1 : 0.f;
+      p2 = (cc + 2 >= lo && cc + 2 < hi) ? p2 : 0.f;
+      p3 = (cc + 3 >= lo && cc + 3 < hi) ? p3 : 0.f;
     }
-    tmem_st32(dst + 32 * hh, pk);
+    p[c] = __float_as_uint(p0);
+    p[c + 1] = __float_as_uint(p1);
+    p[c + 2] = __float_as_uint(p2);
+    p[c + 3] = __float_as_uint(p3);
   }
-  tmem_wait_st();
 }
 
-// The mask is skipped when no lane of the warp needs it (the tensor-memory
-// accesses must stay warp-uniform).
+// The mask is skipped when no lane of the warp needs it for these columns
+// (the tensor-memory accesses must stay warp-uniform).
 template <typename Src>
-__device__ __forceinline__ void p_from_s(uint32_t t_s, uint32_t dst, int lo, int hi, float sl2, Src nlse2) {
-  if (__all_sync(0xffffffffu, lo <= 0 && hi >= 128)) p_from_s_impl<false>(t_s, dst, lo, hi, sl2, nlse2);
-  else p_from_s_impl<true>(t_s, dst, lo, hi, sl2, nlse2);
+__device__ __forceinline__ void p_half(int c0, int lo, int hi, float sl2, Src nlse2, uint32_t (&p)[64]) {
+  if (__all_sync(0xffffffffu, lo <= c0 && hi >= c0 + 64)) p_half_impl<false>(c0, lo, hi, sl2, nlse2, p);
+  else p_half_impl<true>(c0, lo, hi, sl2, nlse2, p);
 }
 
-// Warpgroup 1's step, given P as 64 packed bf16 pairs: dS = P (dP scale +
-// ndsc) with ndsc = -D scale, i.e. P (dP - D) scale, for 128 columns, packed
-// into the first 64 columns of dP (chunk c of 32 dP columns writes packed
-// columns 16c .. 16c+15, already read).
+// 64 fp32 values as 32 bf16 pairs into 32 tensor-memory columns.
+__device__ __forceinline__ void store_pairs32(uint32_t dst, const uint32_t (&v)[64]) {
+  uint32_t pk[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
+  tmem_st32(dst, pk);
+}
+
+// dS = P (dP scale + ndsc) with ndsc = -D scale, i.e. P (dP - D) scale, for
+// the same 64 columns (dP at t_dp, column c0 of the operand), written as 32
+// bf16-pair columns at t_dp: chunk h of 32 dP columns writes packed columns
+// 16h .. 16h+15, which chunk 0 has already read.
 template <typename Src>
-__device__ __forceinline__ void ds_from_dp(uint32_t t_dp, const uint32_t (&pp)[64], float scale, Src ndsc) {
+__device__ __forceinline__ void ds_half(uint32_t t_dp, int c0, const uint32_t (&p)[64], float scale, Src ndsc) {
   const uint64_t sc2 = f2_pack(scale, scale);
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
+  for (int hh = 0; hh < 2; ++hh) {
     uint32_t dp[32];
-    tmem_ld32_sync(t_dp + 32 * ch, dp);
+    tmem_ld32_sync(t_dp + 32 * hh, dp);
     uint32_t pk[16];
 #pragma unroll
     for (int c = 0; c < 32; c += 4) {
-      const int q = 32 * ch + c;
+      const int q = 32 * hh + c;
       uint64_t n01, n23;
-      ndsc.pair4(q, n01, n23);
-      const uint32_t w0 = pp[q >> 1], w1 = pp[(q >> 1) + 1];
+      ndsc.pair4(c0 + q, n01, n23);
       const uint64_t t01 = f2_fma(f2_pack(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), sc2, n01);
       const uint64_t t23 = f2_fma(f2_pack(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), sc2, n23);
-      const uint64_t d01 = f2_mul(f2_pack(bf16_lo(w0), bf16_hi(w0)), t01);
-      const uint64_t d23 = f2_mul(f2_pack(bf16_lo(w1), bf16_hi(w1)), t23);
+      const uint64_t d01 = f2_mul(f2_pack(__uint_as_float(p[q]), __uint_as_float(p[q + 1])), t01);
+      const uint64_t d23 = f2_mul(f2_pack(__uint_as_float(p[q + 2]), __uint_as_float(p[q + 3])), t23);
       float s0, s1, s2, s3;
       f2_unpack(d01, s0, s1);
       f2_unpack(d23, s2, s3);
       pk[c >> 1] = pack_bf16x2(s0, s1);
       pk[(c >> 1) + 1] = pack_bf16x2(s2, s3);
     }
-    tmem_st16(t_dp + 16 * ch, pk);
+    tmem_st16(t_dp + 16 * hh, pk);
   }
-  tmem_wait_st();
 }
 
 // ------------------------------------------------------------------ D_i
@@ -298,7 +301,7 @@ struct KVCfg : BCfg<D> {
 };
 
 enum { KB_KV_FULL = 0, KB_KV_EMPTY = 1, KB_QD_FULL = 2, KB_QD_EMPTY = 4, KB_S_FULL = 6, KB_DP_FULL = 7,
-       KB_P_FULL = 8, KB_P_READ = 9, KB_DS_FULL = 10, KB_ACC_FULL = 11, KB_ACC_EMPTY = 12, KB_DRAIN = 13 };
+       KB_P_FULL = 8, KB_DS_FULL = 9, KB_ACC_FULL = 10, KB_ACC_EMPTY = 11, KB_DRAIN = 12 };
 
 struct KVUnit {
   int k0, k1, hk;  // keys [k0, k1) of key/value head hk
@@ -350,9 +353,8 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     mbar_init(bar(KB_S_FULL), 1);
     mbar_init(bar(KB_DP_FULL), 1);
-    mbar_init(bar(KB_P_FULL), 4);
-    mbar_init(bar(KB_P_READ), 4);
-    mbar_init(bar(KB_DS_FULL), 4);
+    mbar_init(bar(KB_P_FULL), 8);   // both compute warpgroups, one arrival per warp
+    mbar_init(bar(KB_DS_FULL), 8);
     mbar_init(bar(KB_ACC_FULL), 1);
     mbar_init(bar(KB_ACC_EMPTY), 8);
     mbar_init(bar(KB_DRAIN), 1);
@@ -460,9 +462,8 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
           tc_fence_after();
           mma_acc<D>(tdV, tS, sq + C::TILE, n > 0);  // dV += P^T dO
           if (more) {
-            // S(g+1) overwrites P^T(g): dV(g) is issued before it, and
-            // warpgroup 1 has read P^T(g).
-            if (!mbar_wait_bounded(bar(KB_P_READ), ph, tmo, f.err, abort_flag)) { ok = false; break; }
+            // S(g+1) overwrites P^T(g): dV(g) is issued before it, and both
+            // warpgroups have read S(g) (they keep P in registers).
             if (!mbar_wait_bounded(bar(KB_QD_FULL + (g + 1) % C::QSTAGE), ((g + 1) / C::QSTAGE) & 1, tmo,
                                    f.err, abort_flag)) { ok = false; break; }
             tc_fence_after();
@@ -490,7 +491,8 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute
-    const int wg = (warp - 4) >> 2;  // 0: S -> P, 1: dP -> dS
+    const int wg = (warp - 4) >> 2;  // warpgroup: columns [64 wg, 64 wg + 64) of every step
+    const int c0 = 64 * wg;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -516,35 +518,30 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         const int q0 = w.qa + 128 * (n / G);
         const uint8_t* stage = smem + C::OFF_QD + (g % C::QSTAGE) * C::STAGE_BYTES + 2 * C::TILE;
         const uint32_t qd_bar = bar(KB_QD_FULL + g % C::QSTAGE), qd_ph = (g / C::QSTAGE) & 1;
-        if (wg == 0) {
-          bool e = mbar_wait_bounded(bar(KB_S_FULL), ph, tmo, f.err, abort_flag);
-          e = e && mbar_wait_bounded(qd_bar, qd_ph, tmo, f.err, abort_flag);
-          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-          tc_fence_after();
-          const int clo = kvalid ? max(lo, q0) - q0 : 0;
-          const int chi = kvalid ? min(hi, q0 + 128) - q0 : 0;
-          p_from_s(tS, tS, clo, chi, sl2, ColVals{reinterpret_cast<const float*>(stage)});
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(KB_P_FULL));
-        } else {
-          bool e = mbar_wait_bounded(bar(KB_P_FULL), ph, tmo, f.err, abort_flag);
-          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t pp[64];
-          tmem_ld64(tS, pp);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(KB_P_READ));
-          e = mbar_wait_bounded(bar(KB_DP_FULL), ph, tmo, f.err, abort_flag);
-          e = e && mbar_wait_bounded(qd_bar, qd_ph, tmo, f.err, abort_flag);
-          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-          tc_fence_after();
-          ds_from_dp(tdP, pp, scale, ColVals{reinterpret_cast<const float*>(stage + 512)});
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(KB_DS_FULL));
-        }
+        // Both warpgroups: P for query columns [c0, c0 + 64), packed into
+        // S columns c0 .. c0+31; then dS for the same columns into dP.
+        bool e = mbar_wait_bounded(bar(KB_S_FULL), ph, tmo, f.err, abort_flag);
+        e = e && mbar_wait_bounded(qd_bar, qd_ph, tmo, f.err, abort_flag);
+        if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+        tc_fence_after();
+        const int clo = kvalid ? max(lo, q0) - q0 : 0;
+        const int chi = kvalid ? min(hi, q0 + 128) - q0 : 0;
+        uint32_t p[64];
+        tmem_ld64(tS + c0, p);
+        p_half(c0, clo, chi, sl2, ColVals{reinterpret_cast<const float*>(stage)}, p);
+        store_pairs32(tS + c0, p);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KB_P_FULL));
+        e = mbar_wait_bounded(bar(KB_DP_FULL), ph, tmo, f.err, abort_flag);
+        if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+        tc_fence_after();
+        ds_half(tdP + c0, c0, p, scale, ColVals{reinterpret_cast<const float*>(stage + 512)});
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KB_DS_FULL));
       }
       if (!ok) break;
       gs += w.n_steps;
@@ -589,11 +586,11 @@ struct QCfg : BCfg<D> {
   static constexpr int N_BARS = 16;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
-  static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_STASH = 384;  // stash: P as 64 bf16-pair columns
+  static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;
 };
 
 enum { QB_Q_FULL = 0, QB_Q_EMPTY = 1, QB_KV_FULL = 2, QB_KV_EMPTY = 4, QB_S_FULL = 6, QB_DP_FULL = 7,
-       QB_P_FULL = 8, QB_P_READ = 9, QB_DS_FULL = 10, QB_ACC_FULL = 11, QB_ACC_EMPTY = 12, QB_DRAIN = 13 };
+       QB_S_READ = 8, QB_DS_FULL = 9, QB_ACC_FULL = 10, QB_ACC_EMPTY = 11, QB_DRAIN = 12 };
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -622,9 +619,8 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     mbar_init(bar(QB_S_FULL), 1);
     mbar_init(bar(QB_DP_FULL), 1);
-    mbar_init(bar(QB_P_FULL), 4);
-    mbar_init(bar(QB_P_READ), 4);
-    mbar_init(bar(QB_DS_FULL), 4);
+    mbar_init(bar(QB_S_READ), 8);   // both compute warpgroups, one arrival per warp
+    mbar_init(bar(QB_DS_FULL), 8);
     mbar_init(bar(QB_ACC_FULL), 1);
     mbar_init(bar(QB_ACC_EMPTY), 8);
     mbar_init(bar(QB_DRAIN), 1);
@@ -729,10 +725,8 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
           const uint32_t skv = sKV + (g % C::KSTAGE) * 2 * C::TILE;
           const uint32_t skv1 = sKV + ((g + 1) % C::KSTAGE) * 2 * C::TILE;
           if (more) {
-            // Warpgroup 1 has read the stashed P(g) (so warpgroup 0, which
-            // starts on S(g+1), may overwrite the stash), and S(g) was read
-            // before P(g) was stashed: S may be overwritten.
-            if (!mbar_wait_bounded(bar(QB_P_READ), ph, tmo, f.err, abort_flag)) { ok = false; break; }
+            // Both warpgroups have read S(g): S may be overwritten.
+            if (!mbar_wait_bounded(bar(QB_S_READ), ph, tmo, f.err, abort_flag)) { ok = false; break; }
             if (!mbar_wait_bounded(bar(QB_KV_FULL + (g + 1) % C::KSTAGE), ((g + 1) / C::KSTAGE) & 1, tmo,
                                    f.err, abort_flag)) { ok = false; break; }
             tc_fence_after();
@@ -760,7 +754,8 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute
-    const int wg = (warp - 4) >> 2;  // 0: S -> P, 1: dP -> dS
+    const int wg = (warp - 4) >> 2;  // warpgroup: columns [64 wg, 64 wg + 64) of every block
+    const int c0 = 64 * wg;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -790,38 +785,30 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       int ka, kb, cls[2];
       while (next_tile(f, cur, qt, ka, kb, cls)) {
         const uint32_t ph = g & 1;
-        const uint32_t stash = tmem + lane_off + C::TM_STASH;
-        if (wg == 0) {
-          // S(g) is issued only after warpgroup 1 read the stash of block g-1.
-          bool e = mbar_wait_bounded(bar(QB_S_FULL), ph, tmo, f.err, abort_flag);
-          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-          tc_fence_after();
-          int lo = 0, hi = 128;
-          if (cls[0] != CLS_FULL) {
-            lo = valid ? max(ka, rds) - ka : 0;
-            hi = valid ? min(kb, rend) - ka : 0;
-          }
-          p_from_s(tS, stash, lo, hi, sl2, RowVal{f2_pack(nlse2, nlse2)});
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(QB_P_FULL));
-        } else {
-          bool e = mbar_wait_bounded(bar(QB_P_FULL), ph, tmo, f.err, abort_flag);
-          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t pp[64];
-          tmem_ld64(stash, pp);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(QB_P_READ));
-          e = mbar_wait_bounded(bar(QB_DP_FULL), ph, tmo, f.err, abort_flag);
-          if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-          tc_fence_after();
-          ds_from_dp(tdP, pp, scale, RowVal{f2_pack(ndsc, ndsc)});
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(QB_DS_FULL));
+        // Both warpgroups: P for key columns [c0, c0 + 64) in registers, then
+        // dS for the same columns into dP.
+        bool e = mbar_wait_bounded(bar(QB_S_FULL), ph, tmo, f.err, abort_flag);
+        if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t p[64];
+        tmem_ld64(tS + c0, p);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_S_READ));
+        int lo = 0, hi = 128;
+        if (cls[0] != CLS_FULL) {
+          lo = valid ? max(ka, rds) - ka : 0;
+          hi = valid ? min(kb, rend) - ka : 0;
         }
+        p_half(c0, lo, hi, sl2, RowVal{f2_pack(nlse2, nlse2)}, p);
+        e = mbar_wait_bounded(bar(QB_DP_FULL), ph, tmo, f.err, abort_flag);
+        if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
+        tc_fence_after();
+        ds_half(tdP + c0, c0, p, scale, RowVal{f2_pack(ndsc, ndsc)});
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_DS_FULL));
         ++g;
         ++nblk;
       }
