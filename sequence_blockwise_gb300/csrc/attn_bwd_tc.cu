@@ -294,14 +294,16 @@ struct KVCfg : BCfg<D> {
   static constexpr int OFF_V = B::TILE;
   static constexpr int OFF_QD = 2 * B::TILE;
   static constexpr int OFF_BAR = OFF_QD + QSTAGE * STAGE_BYTES;
-  static constexpr int N_BARS = 16;
-  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+  static constexpr int N_BARS = 17;
+  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;  // TMEM address, abort flag, unit ring[2]
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
 };
 
 enum { KB_KV_FULL = 0, KB_KV_EMPTY = 1, KB_QD_FULL = 2, KB_QD_EMPTY = 4, KB_S_FULL = 6, KB_DP_FULL = 7,
-       KB_P_FULL = 8, KB_DS_FULL = 9, KB_ACC_FULL = 10, KB_ACC_EMPTY = 11, KB_DRAIN = 12 };
+       KB_P_FULL = 8, KB_DS_FULL = 9, KB_ACC_FULL = 10, KB_ACC_EMPTY = 11, KB_DRAIN = 12, KB_U_FULL = 13,
+       KB_U_EMPTY = 15 };
+constexpr int KV_UNIT_CONSUMERS = 9;  // the MMA lane and the eight compute warps
 
 struct KVUnit {
   int k0, k1, hk;  // keys [k0, k1) of key/value head hk
@@ -309,7 +311,9 @@ struct KVUnit {
   int n_steps;     // 128-row Q tiles in [qa, qb) times the heads of the group
 };
 
-// Units are head-major: all key tiles of head 0, then head 1, ...
+// Units are head-major: all key tiles of head 0, then head 1, ...; within a
+// head the key tiles in order, which for causal masks is longest first. CTAs
+// claim units from an atomic counter in that order.
 __device__ __forceinline__ KVUnit kv_unit(const AttnArgs& a, int u) {
   KVUnit w;
   const int n_tiles = (a.T + 127) / 128;
@@ -340,6 +344,7 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* uring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const AttnArgs& f = a.fwd;
@@ -347,6 +352,10 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   if (threadIdx.x == 0) {
     mbar_init(bar(KB_KV_FULL), 1);
     mbar_init(bar(KB_KV_EMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(KB_U_FULL + s), 1);
+      mbar_init(bar(KB_U_EMPTY + s), KV_UNIT_CONSUMERS);
+    }
     for (int s = 0; s < C::QSTAGE; ++s) {
       mbar_init(bar(KB_QD_FULL + s), 32);  // one asynchronous arrival per producer lane
       mbar_init(bar(KB_QD_EMPTY + s), 1);
@@ -379,7 +388,25 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     int armed_kv = 0, armed_qd[C::QSTAGE] = {0, 0};
     uint32_t par_kv = 0, par_qd[C::QSTAGE] = {0, 0};
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+    int uslot = 0;
+    uint32_t uph = 0;
+    for (;; ++unit_cnt) {
+      // Claim the next unit and hand its id to the other roles (-1: done).
+      int u = 0;
+      bool pub = true;
+      if (lane == 0) {
+        u = atomicAdd(a.unit_counter, 1);
+        if (u >= n_units) u = -1;
+        pub = mbar_wait_bounded(bar(KB_U_EMPTY + uslot), uph ^ 1, tmo, f.err, abort_flag);
+        if (pub) {
+          uring[uslot] = u;
+          mbar_arrive(bar(KB_U_FULL + uslot));
+        }
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!__shfl_sync(0xffffffffu, pub ? 1 : 0, 0)) { ok = false; break; }
+      if (++uslot == 2) { uslot = 0; uph ^= 1; }
+      if (u < 0) break;
       const KVUnit w = kv_unit(f, u);
       bool got = true;
       if (lane == 0) {
@@ -435,7 +462,14 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       const uint32_t tdV = tmem + C::TM_DV, tdK = tmem + C::TM_DK;
       uint32_t unit_cnt = 0, gs = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+      int uslot = 0;
+      uint32_t uph = 0;
+      for (;; ++unit_cnt) {
+        if (!mbar_wait_bounded(bar(KB_U_FULL + uslot), uph, tmo, f.err, abort_flag)) { ok = false; break; }
+        const int u = uring[uslot];
+        mbar_arrive(bar(KB_U_EMPTY + uslot));
+        if (++uslot == 2) { uslot = 0; uph ^= 1; }
+        if (u < 0) break;
         const KVUnit w = kv_unit(f, u);
         if (!mbar_wait_bounded(bar(KB_KV_FULL), unit_cnt & 1, tmo, f.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -502,7 +536,16 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     const float sl2 = f.scale_log2, scale = f.scale;
     uint32_t unit_cnt = 0, gs = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
+    int uslot = 0;
+    uint32_t uph = 0;
+    for (;; ++unit_cnt) {
+      const bool eu = mbar_wait_bounded(bar(KB_U_FULL + uslot), uph, tmo, f.err, abort_flag);
+      if (!__all_sync(0xffffffffu, eu)) { ok = false; break; }
+      const int u = uring[uslot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(KB_U_EMPTY + uslot));
+      if (++uslot == 2) { uslot = 0; uph ^= 1; }
+      if (u < 0) break;
       const KVUnit w = kv_unit(f, u);
       const int j = w.k0 + r;
       const bool kvalid = j < w.k1;

@@ -302,6 +302,9 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   b.lse = lse;
   b.ndsc = dvec;
   b.nlse2 = lse2;
+  // Header word 4 is free in the set-up kernel's layout: the dK/dV queue.
+  b.unit_counter = static_cast<int32_t*>(workspace) + 4;
+  if (cudaMemsetAsync(b.unit_counter, 0, sizeof(int32_t), st) != cudaSuccess) return SP_ERR_CUDA;
   b.dq = dq;
   b.dk = dk;
   b.dv = dv;

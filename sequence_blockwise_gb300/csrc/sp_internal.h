@@ -66,6 +66,7 @@ struct BwdArgs {
   const float* lse;    // [Hq][T] natural-log LSE written by the forward
   const float* ndsc;   // [Hq][T] -scale * D_i, D_i = dO_i . O_i
   const float* nlse2;  // [Hq][T] -LSE_i * log2(e)
+  int32_t* unit_counter;  // dK/dV work-unit queue (zeroed before the launch)
   void* dq;           // bf16 [T][Hq][d]
   void* dk;           // bf16 [T][Hkv][d]
   void* dv;           // bf16 [T][Hkv][d]
