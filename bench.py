@@ -312,7 +312,40 @@ def run_ours(args, world, rank, local):
                "kernels": "bwd_rowdot, prep_kernel, bwd_dq_kernel<128>, bwd_dkdv_kernel<128>"}
         del dout, dq, dk, dv
 
+    # ---- secondary: the log-sum-exp merge kernel of the unfused API path,
+    # bandwidth bound (12 bytes per O element + 12 per LSE word). Shape of the
+    # 64K full-mask layer's partials over all rows at once, so that the three
+    # fp32 O arrays (512 MB each) are far larger than L2.
+    merge = None
+    if not args.no_backward:
+        wm = wl.WORKLOADS[3]
+        rows, Hm, dm = wm.T, wm.Hq, wm.d
+        o_acc = torch.randn((rows, Hm, dm), dtype=torch.float32, device=dev)
+        o_part = torch.randn((rows, Hm, dm), dtype=torch.float32, device=dev)
+        l_acc = torch.randn((Hm, rows), dtype=torch.float32, device=dev)
+        l_part = torch.randn((Hm, rows), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            sb.sp_lse_merge(o_acc, l_acc, o_part, l_part, stream=stream)
+        torch.cuda.synchronize(dev)
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_m = 10
+        m0.record(stream)
+        for _ in range(n_m):
+            sb.sp_lse_merge(o_acc, l_acc, o_part, l_part, stream=stream)
+        m1.record(stream)
+        torch.cuda.synchronize(dev)
+        sb.sp_check_device_status(stream)
+        m_ms = m0.elapsed_time(m1) / n_m
+        m_bytes = 12 * o_acc.numel() + 12 * l_acc.numel()
+        merge = {"kernel": "lse_merge_kernel", "bound": "hbm", "achieved": round(m_bytes / (m_ms * 1e-3) / 1e9, 1),
+                 "unit": "GB/s", "bytes_per_call": int(m_bytes), "ms_per_call": round(m_ms, 4),
+                 "shape": f"partials [{rows}, {Hm}, {dm}] fp32 + LSE [{Hm}, {rows}] ({wm.name})"}
+        del o_acc, o_part, l_acc, l_part
+
     peaks = read_peaks()
+    if merge is not None:
+        merge["peak"] = peaks["hbm_gbs"]
+        merge["frac"] = round(merge["achieved"] / peaks["hbm_gbs"], 4)
     if bwd is not None:
         bwd["frac_of_peak"] = round(bwd["tflops"] / peaks["bf16_tflops"], 4)
     avg_launch_ms = sum(per) / len(per)
@@ -357,6 +390,7 @@ def run_ours(args, world, rank, local):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "backward": bwd,
+            "secondary_roofline": merge,
         }
     return result, w, cu
 

@@ -193,6 +193,26 @@ sp_status sp_schedule_link_bytes(sp_sched_kind kind, int32_t P, int32_t total_to
                                  uint64_t seed, int64_t bytes_per_token, int32_t needed_only,
                                  int64_t* out);
 
+/* sp_schedule_link_bytes_hier — host only; communication volume of a
+ * two-level schedule (sp_schedule_build_hier) on P = R * U virtual ranks,
+ * inputs in `elem_bytes`-byte elements.
+ *  intra[u*P + v] (int64 [P*P]): bytes over the directed link u -> v of the
+ *    Intra-SP all-to-all of one attention call: rank g*U+u first holds the
+ *    u-th of U equal parts of group g's tokens (all heads); it sends Q of
+ *    query-head slice u' and K, V of the key/value heads slice u' needs to
+ *    rank g*U+u' (u' != u), and receives O of slice u' for its tokens back.
+ *    (Group chunks: the equal RING/TASP split, or the ZIGZAG pair.)
+ *  inter[(t-1)*P*P + u*P + v] (int64 [(R-1)*P*P], unused for R == 1): the
+ *    Inter-SP transfers per iteration t, as sp_schedule_link_bytes for the
+ *    R groups, carried separately between the ranks of each head slice with
+ *    that slice's key/value heads (bytes per token 2 * kv_heads * d * elem_bytes).
+ *  Head slices must cover whole key/value-head groups or lie inside one
+ *  (SP_ERR_UNSUPPORTED otherwise). */
+sp_status sp_schedule_link_bytes_hier(sp_sched_kind inter_kind, int32_t R, int32_t U, int32_t total_tokens,
+                                      const int32_t* cu_seqlens_host, int32_t ndocs, int32_t causal,
+                                      uint64_t seed, int32_t Hq, int32_t Hkv, int32_t d, int32_t elem_bytes,
+                                      int32_t needed_only, int64_t* intra, int64_t* inter);
+
 /* sp_partial_attn — one partial attention step ("partial attention
  * computation", HSAP abstract; one iteration of Ring Attention, TASP abstract).
  * For every query row t in [q_begin, q_end) and head h, over the keys

@@ -80,6 +80,11 @@ def _load():
                                                    ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, i32p,
                                                    i32p, ctypes.c_longlong, i32p, ctypes.c_int,
                                                    ctypes.c_char_p, ctypes.c_int, i32p]
+        lib.oracle_link_bytes_hier.restype = ctypes.c_int
+        lib.oracle_link_bytes_hier.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                               ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)]
         lib.oracle_chunk_bounds.restype = ctypes.c_int
         lib.oracle_chunk_bounds.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
                                             ctypes.c_int, i32p]
@@ -302,6 +307,25 @@ def check_hier_schedule(kind: int, R: int, U: int, Hq: int, T: int, cu_seqlens, 
     rc = lib.oracle_check_hier_schedule(kind, R, U, Hq, T, cup, len(cu) - 1, int(causal), itp, hdp, len(it),
                                         scp, int(brute), buf, 256, bp)
     return int(rc), buf.value.decode()
+
+
+def link_bytes_hier(kind: int, R: int, U: int, T: int, cu_seqlens, causal: bool, Hq: int, Hkv: int, d: int,
+                    elem_bytes: int = 2, succ=None, needed_only: bool = False):
+    """Two-level communication restated per token and head: (intra [P, P], inter [R-1, P, P])."""
+    lib = _load()
+    cu, cup = _i32(cu_seqlens)
+    if succ is None:
+        succ = np.zeros((max(R - 1, 1), max(R, 1)), dtype=np.int32)
+    sc, scp = _i32(succ)
+    P = R * U
+    intra = np.zeros((P, P), dtype=np.int64)
+    inter = np.zeros((max(R - 1, 1), P, P), dtype=np.int64)
+    ll = ctypes.POINTER(ctypes.c_longlong)
+    rc = lib.oracle_link_bytes_hier(kind, R, U, T, cup, len(cu) - 1, int(causal), scp, Hq, Hkv, d, elem_bytes,
+                                    int(needed_only), intra.ctypes.data_as(ll), inter.ctypes.data_as(ll))
+    if rc != 0:
+        raise ValueError(f"oracle_link_bytes_hier rejected its arguments (code {rc})")
+    return intra, inter[:max(R - 1, 0)]
 
 
 def chunk_bounds(mode: int, P: int, T: int, cu_seqlens, causal: bool):

@@ -492,6 +492,88 @@ int oracle_check_schedule(int kind, int P, int T, const int32_t* cu, int ndocs, 
   return 0;
 }
 
+int oracle_link_bytes(int kind, int P, int T, const int32_t* cu, int ndocs, int causal,
+                      const int32_t* succ, long long bytes_per_token, int needed_only,
+                      long long* out);
+
+// Communication of a two-level schedule, restated token by token and head by
+// head: token t belongs to group g (its chunk of the R-way split, or the pair
+// of the 2R-way split for zigzag) and, by its position in the group's tokens
+// cut into U parts, to rank g*U + u. For every query head h of a slice u'
+// != u the token's q (before) and o (after) cross the links u -> u' and
+// u' -> u; for every key/value head a slice u' != u uses, its k and v cross
+// u -> u'. The Inter-SP part is oracle_link_bytes of the R groups, with the
+// key/value heads each slice uses, placed on the links between the ranks of
+// that slice. Output layout as the library's sp_schedule_link_bytes_hier.
+int oracle_link_bytes_hier(int kind, int R, int U, int T, const int32_t* cu, int ndocs, int causal,
+                           const int32_t* succ, int Hq, int Hkv, int d, int eb, int needed_only,
+                           long long* intra, long long* inter) {
+  if (R < 1 || U < 1 || Hq % U != 0 || Hq % Hkv != 0) return 1;
+  if (oracle_check_cu_seqlens(cu, ndocs, T) != 0) return 2;
+  const int P = R * U, hs = Hq / U, G = Hq / Hkv;
+  const size_t PP = static_cast<size_t>(P) * P;
+  for (size_t i = 0; i < PP; ++i) intra[i] = 0;
+  // Tokens of each group, in token order.
+  std::vector<std::vector<int>> toks(R);
+  for (int t = 0; t < T; ++t) {
+    int g;
+    if (kind == 1) {
+      const int c = t / (T / (2 * R));
+      g = c < R ? c : 2 * R - 1 - c;
+    } else {
+      g = 0;
+      for (int x = 0; x < R; ++x) {
+        int b, e;
+        split_bounds(T, R, x, &b, &e);
+        if (t >= b && t < e) g = x;
+      }
+    }
+    toks[g].push_back(t);
+  }
+  // Key/value heads used by each slice.
+  std::vector<std::vector<int>> uses(U, std::vector<int>(Hkv, 0));
+  for (int h = 0; h < Hq; ++h) uses[h / hs][h / G] = 1;
+  for (int g = 0; g < R; ++g) {
+    const int n_g = static_cast<int>(toks[g].size());
+    for (int p = 0; p < n_g; ++p) {
+      int u = 0;
+      for (int x = 0; x < U; ++x) {
+        int b, e;
+        split_bounds(n_g, U, x, &b, &e);
+        if (p >= b && p < e) u = x;
+      }
+      const int owner = g * U + u;
+      for (int h = 0; h < Hq; ++h) {
+        const int v = h / hs;
+        if (v == u) continue;
+        intra[static_cast<size_t>(owner) * P + (g * U + v)] += static_cast<long long>(d) * eb;  // q
+        intra[static_cast<size_t>(g * U + v) * P + owner] += static_cast<long long>(d) * eb;    // o
+      }
+      for (int v = 0; v < U; ++v) {
+        if (v == u) continue;
+        for (int kvh = 0; kvh < Hkv; ++kvh)
+          if (uses[v][kvh]) intra[static_cast<size_t>(owner) * P + (g * U + v)] += 2LL * d * eb;  // k, v
+      }
+    }
+  }
+  if (R == 1) return 0;
+  for (size_t i = 0; i < static_cast<size_t>(R - 1) * PP; ++i) inter[i] = 0;
+  std::vector<long long> grp(static_cast<size_t>(R - 1) * R * R);
+  for (int v = 0; v < U; ++v) {
+    long long nkv = 0;
+    for (int kvh = 0; kvh < Hkv; ++kvh) nkv += uses[v][kvh];
+    const int rc = oracle_link_bytes(kind, R, T, cu, ndocs, causal, succ, 2 * nkv * d * eb, needed_only,
+                                     grp.data());
+    if (rc != 0) return 10 + rc;
+    for (int t = 0; t < R - 1; ++t)
+      for (int a = 0; a < R; ++a)
+        for (int b = 0; b < R; ++b)
+          inter[static_cast<size_t>(t) * PP + static_cast<size_t>(a * U + v) * P + (b * U + v)] =
+              grp[static_cast<size_t>(t) * R * R + static_cast<size_t>(a) * R + b];
+  }
+  return 0;
+}
+
 // Checks a two-level schedule on P = R * U ranks (Inter-SP schedule of kind
 // `kind` over R groups; inside group g, rank g*U + u takes query heads
 // [u Hq/U, (u+1) Hq/U)): every item's head range must be its rank's slice,

@@ -26,6 +26,7 @@ _STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_
            4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_INTERNAL"}
 
 EXPORTED = ["sp_schedule_build", "sp_schedule_build_chunked", "sp_schedule_build_hier", "sp_chunk_bounds",
+            "sp_schedule_link_bytes_hier",
             "sp_tasp_cycles", "sp_packed_attention_ex", "sp_schedule_link_bytes", "sp_partial_attn", "sp_lse_merge",
             "sp_packed_attention_workspace_size", "sp_packed_attention",
             "sp_packed_attention_static_ws", "sp_packed_attention_backward_workspace_size",
@@ -63,6 +64,9 @@ def load():
         lib.sp_schedule_build_chunked.restype = ctypes.c_int
         lib.sp_schedule_build_chunked.argtypes = [ctypes.c_int, i32, i32, vp, i32, i32, u64, vp, vp,
                                                   ctypes.POINTER(ctypes.c_int64)]
+        lib.sp_schedule_link_bytes_hier.restype = ctypes.c_int
+        lib.sp_schedule_link_bytes_hier.argtypes = [ctypes.c_int, i32, i32, i32, vp, i32, i32, u64, i32, i32,
+                                                    i32, i32, i32, vp, vp]
         lib.sp_schedule_build_hier.restype = ctypes.c_int
         lib.sp_schedule_build_hier.argtypes = [ctypes.c_int, i32, i32, i32, vp, i32, i32, u64, i32, vp, vp,
                                                vp, ctypes.POINTER(ctypes.c_int64)]
@@ -154,6 +158,22 @@ def sp_schedule_build_hier(inter_kind: int, R: int, U: int, total_tokens: int, c
                                       Hq, bp, items.ctypes.data, heads.ctypes.data, ctypes.byref(cap)),
            "sp_schedule_build_hier")
     return items[:cap.value], heads[:cap.value]
+
+
+def sp_schedule_link_bytes_hier(inter_kind: int, R: int, U: int, total_tokens: int, cu_seqlens, causal: bool,
+                                Hq: int, Hkv: int, d: int, elem_bytes: int = 2, seed: int = 0,
+                                needed_only: bool = False):
+    """Two-level communication model: (intra [P, P], inter [R-1, P, P]) bytes per directed link."""
+    lib = load()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    P = R * U
+    intra = np.zeros((P, P), dtype=np.int64)
+    inter = np.zeros((max(R - 1, 0), P, P), dtype=np.int64)
+    _check(lib.sp_schedule_link_bytes_hier(inter_kind, R, U, total_tokens, cu.ctypes.data, len(cu) - 1,
+                                           int(causal), seed, Hq, Hkv, d, elem_bytes, int(needed_only),
+                                           intra.ctypes.data, inter.ctypes.data if inter.size else None),
+           "sp_schedule_link_bytes_hier")
+    return intra, inter
 
 
 SP_CHUNK_EQUAL, SP_CHUNK_BALANCED, SP_CHUNK_BALANCED_DOC = 0, 1, 2

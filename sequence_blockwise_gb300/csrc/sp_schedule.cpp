@@ -633,3 +633,63 @@ extern "C" sp_status sp_schedule_link_bytes(sp_sched_kind kind, int32_t P, int32
   }
   return SP_OK;
 }
+
+extern "C" sp_status sp_schedule_link_bytes_hier(sp_sched_kind inter_kind, int32_t R, int32_t U, int32_t T,
+                                                 const int32_t* cu, int32_t ndocs, int32_t causal_i,
+                                                 uint64_t seed, int32_t Hq, int32_t Hkv, int32_t d,
+                                                 int32_t elem_bytes, int32_t needed_only, int64_t* intra,
+                                                 int64_t* inter) {
+  if (R < 1 || U < 1 || T < 1 || Hq < 1 || Hkv < 1 || d < 1 || elem_bytes < 1) return SP_ERR_INVALID_ARG;
+  if (Hq % U != 0 || Hq % Hkv != 0) return SP_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(R) * U > 4096) return SP_ERR_INVALID_ARG;
+  const int P = R * U, hs = Hq / U, G = Hq / Hkv;
+  if (!((hs >= G && hs % G == 0) || (hs < G && G % hs == 0))) return SP_ERR_UNSUPPORTED;
+  if (!valid_cu(cu, ndocs, T)) return SP_ERR_INVALID_ARG;
+  if (!intra || (R > 1 && !inter)) return SP_ERR_INVALID_ARG;
+  if (inter_kind == SP_SCHED_ZIGZAG && T % (2 * R) != 0) return SP_ERR_UNSUPPORTED;
+  const int kvs = hs >= G ? hs / G : 1;  // key/value heads one head slice needs
+  const int64_t eb = elem_bytes;
+  const size_t PP = static_cast<size_t>(P) * P;
+  for (size_t i = 0; i < PP; ++i) intra[i] = 0;
+  // Intra-SP all-to-all: rank g*U+u holds the u-th of U equal parts of group
+  // g's tokens (all heads); it sends Q of query slice u' and K, V of the
+  // key/value heads slice u' needs to rank g*U+u', and gets O of slice u' for
+  // its own tokens back.
+  for (int g = 0; g < R; ++g) {
+    int gb, ge;
+    if (inter_kind == SP_SCHED_ZIGZAG) {
+      gb = 0;
+      ge = 2 * (T / (2 * R));
+    } else {
+      split_bounds(T, R, g, &gb, &ge);
+    }
+    const int n_g = ge - gb;
+    for (int u = 0; u < U; ++u) {
+      int sb_, se_;
+      split_bounds(n_g, U, u, &sb_, &se_);
+      const int64_t n = se_ - sb_;
+      for (int v = 0; v < U; ++v) {
+        if (v == u) continue;
+        intra[static_cast<size_t>(g * U + u) * P + (g * U + v)] += n * (hs + 2 * kvs) * d * eb;
+        intra[static_cast<size_t>(g * U + v) * P + (g * U + u)] += n * hs * d * eb;
+      }
+    }
+  }
+  if (R == 1) return SP_OK;
+  // Inter-SP: the R-group schedule moves, for every head slice separately,
+  // the key/value heads of that slice between the ranks of that slice.
+  std::vector<int64_t> grp(static_cast<size_t>(R - 1) * R * R);
+  const sp_status st = sp_schedule_link_bytes(inter_kind, R, T, cu, ndocs, causal_i, seed,
+                                              2 * kvs * static_cast<int64_t>(d) * eb, needed_only, grp.data());
+  if (st != SP_OK) return st;
+  for (size_t i = 0; i < static_cast<size_t>(R - 1) * PP; ++i) inter[i] = 0;
+  for (int t = 0; t < R - 1; ++t)
+    for (int a = 0; a < R; ++a)
+      for (int b = 0; b < R; ++b) {
+        const int64_t x = grp[static_cast<size_t>(t) * R * R + static_cast<size_t>(a) * R + b];
+        if (!x) continue;
+        for (int u = 0; u < U; ++u)
+          inter[static_cast<size_t>(t) * PP + static_cast<size_t>(a * U + u) * P + (b * U + u)] = x;
+      }
+  return SP_OK;
+}

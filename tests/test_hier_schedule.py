@@ -92,3 +92,40 @@ def test_hier_argument_errors():
     with pytest.raises(sb.SpError) as e:
         sb.sp_schedule_build_hier(sb.SP_SCHED_RING, 0, 2, 256, cu, True, 8)
     assert e.value.code == 1
+
+
+# ------------------------------------------------------------------ communication
+
+@pytest.mark.parametrize("kind,R,U,Hq,Hkv,causal,needed", [
+    (sb.SP_SCHED_RING, 2, 8, 16, 16, False, False), (sb.SP_SCHED_TASP, 3, 2, 8, 2, True, True),
+    (sb.SP_SCHED_ZIGZAG, 2, 4, 8, 2, True, False), (sb.SP_SCHED_RING, 4, 2, 8, 8, True, True),
+    (sb.SP_SCHED_RING, 1, 4, 8, 8, True, False), (sb.SP_SCHED_TASP, 5, 4, 32, 8, True, False)])
+def test_hier_link_bytes_match_oracle(kind, R, U, Hq, Hkv, causal, needed):
+    T = 720
+    cu = np.array([0, 130, 131, 400, 720], dtype=np.int32)
+    succ = _succ(kind, R, 3)
+    a = sb.sp_schedule_link_bytes_hier(kind, R, U, T, cu, causal, Hq, Hkv, 64, 2, seed=3, needed_only=needed)
+    b = oracle.link_bytes_hier(kind, R, U, T, cu, causal, Hq, Hkv, 64, 2, succ=succ, needed_only=needed)
+    assert np.array_equal(a[0], b[0])
+    assert np.array_equal(a[1], b[1])
+
+
+def test_hier_link_bytes_closed_forms():
+    """One group: no Inter-SP traffic, and each rank sends its T/U tokens' q and
+    k, v of the other slices' heads and gets o back (hand count). One rank per
+    group: no all-to-all, Inter-SP equals the flat model."""
+    T, U, Hq, Hkv, d = 512, 4, 8, 2, 64
+    cu = np.array([0, 512], dtype=np.int32)
+    intra, inter = sb.sp_schedule_link_bytes_hier(sb.SP_SCHED_RING, 1, U, T, cu, True, Hq, Hkv, d, 2)
+    assert inter.shape[0] == 0
+    n = T // U
+    hs, kvs = Hq // U, 1      # 2 query heads per slice, inside one KV group of 4
+    for u in range(U):
+        for v in range(U):
+            want = 0 if u == v else n * (hs + 2 * kvs) * d * 2 + n * hs * d * 2
+            assert intra[u, v] == want, (u, v)
+    R = 4
+    intra, inter = sb.sp_schedule_link_bytes_hier(sb.SP_SCHED_RING, R, 1, T, cu, True, Hq, Hkv, d, 2)
+    assert not intra.any()
+    flat = sb.sp_schedule_link_bytes(sb.SP_SCHED_RING, R, T, cu, True, bytes_per_token=2 * Hkv * d * 2)
+    assert np.array_equal(inter, flat)
