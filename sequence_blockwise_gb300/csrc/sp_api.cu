@@ -279,15 +279,16 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   if (!encoder()) return SP_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const sp::WsLayout L = sp::ws_layout(n_items);
-  float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.total);
-  float* lse2 = reinterpret_cast<float*>(
+  // After the set-up kernel's layout: -scale D and -LSE log2 e, [Hq][T] fp32 each.
+  float* ndsc = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.total);
+  float* nlse2 = reinterpret_cast<float*>(
       static_cast<char*>(workspace) + L.total +
       ((static_cast<size_t>(T) * Hq * sizeof(float) + 255) & ~static_cast<size_t>(255)));
 
   const long long warps = static_cast<long long>(T) * Hq;
   long long g = (warps + 7) / 8;
   if (g > static_cast<long long>(sms) * 16) g = static_cast<long long>(sms) * 16;
-  cudaError_t e = sp::launch_bwd_rowdot(o, dout, lse, dvec, lse2, T, Hq, d, scale, static_cast<int>(g), st);
+  cudaError_t e = sp::launch_bwd_rowdot(o, dout, lse, ndsc, nlse2, T, Hq, d, scale, static_cast<int>(g), st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
   e = sp::launch_prep(items_dev, nullptr, n_items, T, Hq, Hkv, sp::BWD_ROWS_PER_UNIT, workspace, err, st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
@@ -300,8 +301,8 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   b.fwd.segs = reinterpret_cast<const sp::SegEntry*>(static_cast<const char*>(workspace) + L.off_segs);
   b.fwd.rows_per_unit = sp::BWD_ROWS_PER_UNIT;
   b.lse = lse;
-  b.ndsc = dvec;
-  b.nlse2 = lse2;
+  b.ndsc = ndsc;
+  b.nlse2 = nlse2;
   // Header word 4 is free in the set-up kernel's layout: the dK/dV queue.
   b.unit_counter = static_cast<int32_t*>(workspace) + 4;
   if (cudaMemsetAsync(b.unit_counter, 0, sizeof(int32_t), st) != cudaSuccess) return SP_ERR_CUDA;
