@@ -259,6 +259,10 @@ size_t sp_packed_attention_workspace_size(int64_t n_items);
  *  workspace: device, at least sp_packed_attention_workspace_size(n_items)
  *     bytes, owned by the caller, reused between calls; calls that share a
  *     workspace must not overlap in time.
+ *  n_items < 2^30 (SP_ERR_INVALID_ARG otherwise). The order in which a unit
+ *  merges its items' partials is free (the log-sum-exp merge is associative):
+ *  items that are not whole 128-key tiles long are visited in key order, and
+ *  contiguous key ranges are walked as one.
  *  An inconsistent item list is reported through sp_check_device_status. */
 sp_status sp_packed_attention(const void* q, const void* k, const void* v, void* o, float* lse,
                               int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,

@@ -707,7 +707,7 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         par_q = unit_cnt & 1;
         load_rows128<D>(sQ, &tmq, bar(QB_Q_FULL), ui.h, ui.q0, f.T);
         load_rows128<D>(sDO, &tmdo, bar(QB_Q_FULL), ui.h, ui.q0, f.T);
-        Cursor cur = make_cursor(ui, qt, f.causal);
+        Cursor cur = make_cursor(f, ui, qt, f.causal);
         int ka, kb, cls[2];
         while (next_tile(f, cur, qt, ka, kb, cls)) {
           const int st = kv_cnt % C::KSTAGE;
@@ -744,7 +744,7 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         tc_fence_after();
         int nblk = 0;
         {
-          Cursor cur = make_cursor(ui, qt, f.causal);
+          Cursor cur = make_cursor(f, ui, qt, f.causal);
           int ka, kb, cls[2];
           while (next_tile(f, cur, qt, ka, kb, cls)) ++nblk;
         }
@@ -824,7 +824,7 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       }
       const int rend = f.causal ? min(rde, t + 1) : rde;
       int nblk = 0;
-      Cursor cur = make_cursor(ui, qt, f.causal);
+      Cursor cur = make_cursor(f, ui, qt, f.causal);
       int ka, kb, cls[2];
       while (next_tile(f, cur, qt, ka, kb, cls)) {
         const uint32_t ph = g & 1;

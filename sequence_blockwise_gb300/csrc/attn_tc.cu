@@ -239,7 +239,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
                         ui.h, ui.q0 + 128 * i);
         // The tile walk runs one tile ahead so that each record can say
         // whether it is the unit's last.
-        Cursor cur = make_cursor(ui, qt, a.causal);
+        Cursor cur = make_cursor(a, ui, qt, a.causal);
         int ka = 0, kb = 0, cls[2] = {0, 0};
         bool have = next_tile(a, cur, qt, ka, kb, cls);
         if (!have) {
@@ -425,7 +425,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       const int rcausal_end = a.causal ? t + 1 : 0x7fffffff;
       float m = NEG_INF, l = 0.f;
       int has_pv = 0;
-      Cursor cur = make_cursor(ui, qt, a.causal);
+      Cursor cur = make_cursor(a, ui, qt, a.causal);
       int ka, kb, cls[2];
       while (next_tile(a, cur, qt, ka, kb, cls)) {
         const int c = wg ? cls[1] : cls[0];

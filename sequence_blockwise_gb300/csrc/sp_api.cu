@@ -214,7 +214,7 @@ sp_status sp_packed_attention_ex(const void* q, const void* k, const void* v, vo
                                  void* stream) {
   sp_status s = check_shapes(T, Hq, Hkv, d, dtype, ndocs, scale);
   if (s != SP_OK) return s;
-  if (n_items < 0 || n_items > 0x7fffffffll) return SP_ERR_INVALID_ARG;
+  if (n_items < 0 || n_items >= (1ll << 30)) return SP_ERR_INVALID_ARG;
   if (T == 0 || n_items == 0) return SP_OK;
   if (!q || !k || !v || !o || !lse || !cu_seqlens_dev || !items_dev || !workspace)
     return SP_ERR_INVALID_ARG;
@@ -232,6 +232,7 @@ sp_status sp_packed_attention_ex(const void* q, const void* k, const void* v, vo
   AttnArgs a = base_args(q, k, v, o, lse, T, Hq, Hkv, d, cu_seqlens_dev, ndocs, causal, scale, err);
   const sp::WsLayout L = sp::ws_layout(n_items);
   a.items = items_dev;
+  a.item_order = reinterpret_cast<const int32_t*>(static_cast<const char*>(workspace) + L.off_order);
   a.header = static_cast<const int32_t*>(workspace);
   a.work_counter = static_cast<int32_t*>(workspace) + sp::WS_COUNTER;
   a.segs = reinterpret_cast<const sp::SegEntry*>(static_cast<const char*>(workspace) + L.off_segs);
@@ -261,7 +262,7 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   sp_status s = check_shapes(T, Hq, Hkv, d, dtype, ndocs, scale);
   if (s != SP_OK) return s;
   if (dtype != SP_DTYPE_BF16) return SP_ERR_UNSUPPORTED;
-  if (n_items < 0 || n_items > 0x7fffffffll) return SP_ERR_INVALID_ARG;
+  if (n_items < 0 || n_items >= (1ll << 30)) return SP_ERR_INVALID_ARG;
   if (T == 0) return SP_OK;
   if (n_items == 0) return SP_ERR_INVALID_ARG;  // a complete schedule has items whenever T > 0
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !cu_seqlens_dev || !items_dev ||
@@ -297,14 +298,14 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   std::memset(&b, 0, sizeof b);
   b.fwd = base_args(q, k, v, nullptr, nullptr, T, Hq, Hkv, d, cu_seqlens_dev, ndocs, causal, scale, err);
   b.fwd.items = items_dev;
+  b.fwd.item_order = reinterpret_cast<const int32_t*>(static_cast<const char*>(workspace) + L.off_order);
   b.fwd.header = static_cast<const int32_t*>(workspace);
   b.fwd.segs = reinterpret_cast<const sp::SegEntry*>(static_cast<const char*>(workspace) + L.off_segs);
   b.fwd.rows_per_unit = sp::BWD_ROWS_PER_UNIT;
   b.lse = lse;
   b.ndsc = ndsc;
   b.nlse2 = nlse2;
-  // Header word 4 is free in the set-up kernel's layout: the dK/dV queue.
-  b.unit_counter = static_cast<int32_t*>(workspace) + 4;
+  b.unit_counter = static_cast<int32_t*>(workspace) + sp::WS_BWD_COUNTER;
   if (cudaMemsetAsync(b.unit_counter, 0, sizeof(int32_t), st) != cudaSuccess) return SP_ERR_CUDA;
   b.dq = dq;
   b.dk = dk;

@@ -43,6 +43,7 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
             int Hkv, int rpu, int32_t* ws, unsigned* err) {
   __shared__ long long scan_tmp[1024];
   __shared__ int bad;
+  __shared__ int any_sorted;
   const WsLayout L = ws_layout(n);
   int32_t* header = ws;
   SegEntry* segs = reinterpret_cast<SegEntry*>(reinterpret_cast<char*>(ws) + L.off_segs);
@@ -50,7 +51,10 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
   int32_t* starts = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + L.off_starts);
   long long* cost = reinterpret_cast<long long*>(reinterpret_cast<char*>(ws) + L.off_cost);
   const int tid = threadIdx.x;
-  if (tid == 0) bad = 0;
+  if (tid == 0) {
+    bad = 0;
+    any_sorted = 0;
+  }
   __syncthreads();
 
   const int chunk = (n + 1023) / 1024;
@@ -88,6 +92,36 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
   if (tid == 0) starts[nseg] = n;
   __syncthreads();
 
+  // Visit order: a group whose items are not all whole 128-key tiles long
+  // (TASP pieces, for example) visits them by key start (ties in schedule
+  // order), so that contiguous key ranges can be walked as one without a cut
+  // tile at each seam. The order of the partial results a unit merges does
+  // not change the result beyond rounding. Other groups, and groups of more
+  // than 2048 items, keep the schedule order. One warp per group.
+  {
+    int32_t* order = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + L.off_order);
+    const int wid = tid >> 5, lid = tid & 31;
+    for (int sg = wid; sg < nseg; sg += 32) {
+      const int g0 = starts[sg], g1 = starts[sg + 1];
+      bool ragged = false;
+      for (int i = g0 + lid; i < g1; i += 32)
+        ragged |= ((__ldg(&items[i].kv_end) - __ldg(&items[i].kv_begin)) & 127) != 0;
+      const bool sort = g1 - g0 <= 2048 && __any_sync(0xffffffffu, ragged);
+      if (sort && lid == 0) any_sorted = 1;
+      for (int i = g0 + lid; i < g1; i += 32) {
+        int rank = i - g0;
+        if (sort) {
+          const int kb = __ldg(&items[i].kv_begin);
+          rank = 0;
+          for (int j = g0; j < g1; ++j) {
+            const int kj = __ldg(&items[j].kv_begin);
+            rank += (kj < kb) || (kj == kb && j < i);
+          }
+        }
+        order[g0 + rank] = i;
+      }
+    }
+  }
   for (int s = tid; s < nseg; s += 1024) {
     const int lo = starts[s], hi = starts[s + 1];
     const sp_item first = items[lo];
@@ -153,6 +187,7 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
     header[WS_N_UNITS] = fail ? 0 : static_cast<int32_t>(total);
     header[WS_STATUS] = fail ? 1 : 0;
     header[WS_COUNTER] = 0;
+    header[WS_ORDERED] = any_sorted;
     if (fail) atomicOr(err, ERR_INTERNAL_BIT);
   }
 }

@@ -61,9 +61,13 @@ __device__ __forceinline__ UnitInfo unit_info(const AttnArgs& a, int u) {
   return ui;
 }
 
-__device__ __forceinline__ void item_range(const AttnArgs& a, int idx, int& kv_b, int& kv_e) {
+// Key range of the idx-th item a unit visits: item order[idx] when a visit
+// order is given, else item idx.
+__device__ __forceinline__ void item_range(const AttnArgs& a, int idx, int& kv_b, int& kv_e,
+                                           const int32_t* order = nullptr) {
   if (a.items) {
-    const int4* p = reinterpret_cast<const int4*>(a.items + idx);
+    const int i = order ? __ldg(order + idx) : idx;
+    const int4* p = reinterpret_cast<const int4*>(a.items + i);
     const int4 hi = __ldg(p + 1);  // q_end, kv_begin, kv_end, flags
     kv_b = hi.y;
     kv_e = hi.z;

@@ -27,7 +27,11 @@ static_assert(sizeof(SegEntry) == 32, "SegEntry is 32 bytes");
 
 // Workspace header (int32 words).
 // WS_COUNTER: next work unit to hand out (reset to 0 by the set-up kernel).
-enum : int { WS_N_SEGS = 0, WS_N_UNITS = 1, WS_STATUS = 2, WS_COUNTER = 3, WS_HEADER_WORDS = 16 };
+// WS_BWD_COUNTER: the backward dK/dV kernel's unit queue.
+// WS_ORDERED: nonzero when some group's items are visited in key order (the
+// set-up kernel's visit order) rather than schedule order.
+enum : int { WS_N_SEGS = 0, WS_N_UNITS = 1, WS_STATUS = 2, WS_COUNTER = 3, WS_BWD_COUNTER = 4,
+             WS_ORDERED = 5, WS_HEADER_WORDS = 16 };
 
 struct AttnArgs {
   const void* q;
@@ -44,6 +48,7 @@ struct AttnArgs {
   // Work description: either a device table produced by the set-up kernel
   // (header != nullptr) or one inline group holding one inline item.
   const sp_item* items;
+  const int32_t* item_order;  // visit order of the items (nullptr: schedule order)
   const SegEntry* segs;
   const int32_t* header;
   int32_t* work_counter;  // dynamic unit queue (nullptr: static striding over CTAs)

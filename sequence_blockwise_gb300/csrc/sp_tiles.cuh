@@ -43,6 +43,11 @@ __device__ __forceinline__ int classify(const QTile& t, int ka, int kb, int caus
   return CLS_MASKED;
 }
 
+// item_end holds the end of the unit's items in its low 30 bits and, in bit
+// 30, whether the items are visited in the set-up kernel's key order (so that
+// the flag costs no register on the per-tile path).
+constexpr int CUR_ORDERED = 1 << 30, CUR_END_MASK = CUR_ORDERED - 1;
+
 struct Cursor {
   int item, item_end, kv_e, k0;
   int lo, hi;  // keys any row of the unit may attend: [lo, hi)
@@ -52,11 +57,13 @@ struct Cursor {
 // keys some row of the unit may attend (the documents of its rows, and keys
 // up to its last row when causal), so that no tile is visited for keys that
 // are masked for every row; tiles start at the clipped start.
-__device__ __forceinline__ Cursor make_cursor(const UnitInfo& ui, const QTile (&qt)[2], int causal) {
-  Cursor c{ui.item_lo, ui.item_hi, 0, 0, 0, 0};
+__device__ __forceinline__ Cursor make_cursor(const AttnArgs& a, const UnitInfo& ui, const QTile (&qt)[2],
+                                              int causal) {
+  const bool ordered = a.header && a.item_order && __ldg(a.header + WS_ORDERED);
+  Cursor c{ui.item_lo, ui.item_hi | (ordered ? CUR_ORDERED : 0), 0, 0, 0, 0};
   const bool e0 = qt[0].qa < qt[0].qb, e1 = qt[1].qa < qt[1].qb;
   if (!e0 && !e1) {
-    c.item = c.item_end;  // no valid row: no tile
+    c.item = ui.item_hi;  // no valid row: no tile
     return c;
   }
   c.lo = e0 ? qt[0].ds : qt[1].ds;
@@ -67,16 +74,30 @@ __device__ __forceinline__ Cursor make_cursor(const UnitInfo& ui, const QTile (&
 
 // Advances to the next 128-key tile of the unit that is not SKIP for both Q
 // tiles. Every role runs this same function, so all agree on the sequence.
+// When the set-up kernel reordered some group (header word WS_ORDERED, read
+// once per unit by make_cursor), items are visited in its key order, and
+// items whose clipped key ranges follow one another without a gap are walked
+// as one range, so that no tile is cut at the seam (TASP pieces of one chunk,
+// for example); otherwise items are walked in schedule order.
 __device__ __forceinline__ bool next_tile(const AttnArgs& a, Cursor& c, const QTile (&qt)[2],
                                           int& ka, int& kb, int (&cls)[2]) {
   while (true) {
     if (c.k0 >= c.kv_e) {
-      if (c.item >= c.item_end) return false;
+      const int end = c.item_end & CUR_END_MASK;
+      if (c.item >= end) return false;
+      const int32_t* order = (c.item_end & CUR_ORDERED) ? a.item_order : nullptr;
       int b, e;
-      item_range(a, c.item, b, e);
+      item_range(a, c.item, b, e, order);
       ++c.item;
       c.k0 = max(b, c.lo);
       c.kv_e = min(e, c.hi);
+      while (order && c.k0 < c.kv_e && c.item < end) {
+        item_range(a, c.item, b, e, order);
+        const int nb = max(b, c.lo), ne = min(e, c.hi);
+        if (nb != c.kv_e || ne <= nb) break;
+        c.kv_e = ne;
+        ++c.item;
+      }
       continue;
     }
     ka = c.k0;

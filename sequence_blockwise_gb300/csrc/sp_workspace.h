@@ -1,5 +1,6 @@
 // Layout of the caller-provided workspace of sp_packed_attention:
-// [header: 16 int32][sorted groups][unsorted groups][group starts][group costs].
+// [header: 16 int32][sorted groups][unsorted groups][group starts][group costs]
+// [item visit order].
 #pragma once
 
 #include <cstddef>
@@ -9,7 +10,7 @@
 namespace sp {
 
 struct WsLayout {
-  size_t off_segs, off_tmp, off_starts, off_cost, total;
+  size_t off_segs, off_tmp, off_starts, off_cost, off_order, total;
 };
 
 __host__ __device__ inline WsLayout ws_layout(long long n) {
@@ -24,6 +25,8 @@ __host__ __device__ inline WsLayout ws_layout(long long n) {
   o = (o + 15) & ~static_cast<size_t>(15);
   L.off_cost = o;
   o += static_cast<size_t>(n) * sizeof(long long);
+  L.off_order = o;
+  o += static_cast<size_t>(n) * sizeof(int32_t);
   L.total = (o + 255) & ~static_cast<size_t>(255);
   return L;
 }
