@@ -241,45 +241,79 @@ def run_ours(args, world, rank, local):
     ms_step = total_ms / args.steps
     value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
 
-    # ---- end to end through the C-ABI with host buffers
+    # ---- end to end through the C-ABI with host buffers: every step copies its
+    # inputs (Q, K, V, cu_seqlens, items) from pinned host memory and reads its O
+    # and LSE back into pinned host memory. Steps are pipelined as a serving
+    # loop would run them: step i+1's inputs travel on one copy stream and step
+    # i-1's outputs on another while step i computes, with two sets of device
+    # buffers.
     qh = q.cpu().pin_memory()
     kh = k.cpu().pin_memory()
     vh = v.cpu().pin_memory()
-    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
     cu_h = torch.from_numpy(cu).pin_memory()
     it_h = torch.from_numpy(att.items).pin_memory()
-    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    oh = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    lh = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
+    qd = [torch.empty_like(q) for _ in range(2)]
+    kd = [torch.empty_like(k) for _ in range(2)]
+    vd = [torch.empty_like(v) for _ in range(2)]
+    od = [torch.empty_like(o) for _ in range(2)]
+    ld = [torch.empty_like(lse) for _ in range(2)]
+    cud = [torch.empty_like(att.cu_dev) for _ in range(2)]
+    itd = [torch.empty_like(att.items_dev) for _ in range(2)]
     h2d = (qh.numel() * qh.element_size() + kh.numel() * kh.element_size() +
            vh.numel() * vh.element_size() + cu_h.numel() * 4 + it_h.numel() * 4)
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    d2h = oh[0].numel() * oh[0].element_size() + lh[0].numel() * lh[0].element_size()
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        att.cu_dev.copy_(cu_h, non_blocking=True)
-        att.items_dev.copy_(it_h, non_blocking=True)
-        sb.sp_packed_attention(qd, kd, vd, o, lse, att.cu_dev, w.causal, att.items_dev,
-                               att.workspace, stream=stream)
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
+    def e2e_run(n_steps, start_ev):
+        s_in.wait_event(start_ev)
+        for i in range(n_steps):
+            sl = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[sl])  # step i-2 has finished reading this slot
+                qd[sl].copy_(qh, non_blocking=True)
+                kd[sl].copy_(kh, non_blocking=True)
+                vd[sl].copy_(vh, non_blocking=True)
+                cud[sl].copy_(cu_h, non_blocking=True)
+                itd[sl].copy_(it_h, non_blocking=True)
+                ev_in[sl].record(s_in)
+            stream.wait_event(ev_in[sl])
+            if i >= 2:
+                stream.wait_event(ev_out[sl])  # step i-2's outputs have left this slot
+            sb.sp_packed_attention(qd[sl], kd[sl], vd[sl], od[sl], ld[sl], cud[sl], w.causal, itd[sl],
+                                   att.workspace, stream=stream)
+            ev_comp[sl].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[sl])
+                oh[sl].copy_(od[sl], non_blocking=True)
+                lh[sl].copy_(ld[sl], non_blocking=True)
+                ev_out[sl].record(s_out)
+        for sl in range(min(2, n_steps)):
+            stream.wait_event(ev_out[sl])
 
-    for _ in range(2):
-        e2e_step()
+    warm = torch.cuda.Event()
+    warm.record(stream)
+    e2e_run(2, warm)
     dist_barrier(world)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps, e0)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     dist_barrier(world)
     e2e_ms = dist_max(e0.elapsed_time(e1), world)
     e2e_value = world * flop * args.steps / (e2e_ms * 1e-3) / 1e12
     sb.sp_check_device_status(stream)
+    # The pipelined result equals the device-resident one.
+    e2e_same = bool(torch.equal(oh[(args.steps - 1) % 2], o.cpu())) if args.steps > 0 else True
 
     # ---- backward of the same call (dQ, dK, dV), timed on its own after the
     # forward's timed region; reported beside the headline, not in `value`.
@@ -386,7 +420,9 @@ def run_ours(args, world, rank, local):
                 "avg_launch_ms": round(avg_launch_ms, 4),
             },
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4),
+                    "pipelined": "inputs of step i+1 and outputs of step i-1 copied during step i",
+                    "matches_device_resident_output": e2e_same},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "backward": bwd,

@@ -185,7 +185,7 @@ sp_status sp_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const 
   unsigned* err;
   int sms;
   if (!device_state(&err, &sms)) return SP_ERR_CUDA;
-  const long long warps = static_cast<long long>(rows) * Hq;
+  const long long warps = (static_cast<long long>(rows) * Hq + 3) / 4;  // 4 (row, head) pairs per warp pass
   long long grid = (warps + 7) / 8;
   if (grid > static_cast<long long>(sms) * 16) grid = static_cast<long long>(sms) * 16;
   return cuda_fail(sp::launch_lse_merge(o_acc, lse_acc, o_part, lse_part, rows, Hq, d,

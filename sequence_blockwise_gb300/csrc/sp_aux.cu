@@ -192,42 +192,65 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
   }
 }
 
-// One warp per (row, head): fold partial 2 into accumulator 1 in place.
+// Folds partial 2 into accumulator 1 in place, by the log-sum-exp rule. Each
+// warp handles UNROLL (row, head) pairs per pass and issues all their O loads
+// before any arithmetic, so that enough bytes are in flight to keep HBM busy
+// (the kernel is bandwidth bound: 12 bytes per O element).
+constexpr int MERGE_UNROLL = 4;
+
 __global__ void __launch_bounds__(256)
 lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
                  const float* __restrict__ o_part, const float* __restrict__ lse_part, int rows,
                  int Hq, int d) {
   const int lane = threadIdx.x & 31;
   const long long n = static_cast<long long>(rows) * Hq;
-  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5) * MERGE_UNROLL;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       w < n; w += wstride) {
-    const int row = static_cast<int>(w / Hq), h = static_cast<int>(w % Hq);
-    const size_t li = static_cast<size_t>(h) * rows + row;
-    const float l1 = lse_acc[li], l2 = __ldg(lse_part + li);
-    const float M = fmaxf(l1, l2);
-    float w1, w2, L;
-    if (M == NEG_INF) {
-      w1 = w2 = 0.f;
-      L = NEG_INF;
-    } else {
-      const float e1 = expf(l1 - M), e2 = expf(l2 - M);
-      const float s = e1 + e2;
-      L = M + logf(s);
-      const float inv = 1.f / s;
-      w1 = e1 * inv;
-      w2 = e2 * inv;
+  const int nv = d >> 2;  // float4 per O row
+  for (long long w0 = (static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * MERGE_UNROLL;
+       w0 < n; w0 += wstride) {
+    // Weights of the UNROLL pairs.
+    float w1[MERGE_UNROLL], w2[MERGE_UNROLL];
+#pragma unroll
+    for (int k = 0; k < MERGE_UNROLL; ++k) {
+      const long long w = w0 + k;
+      w1[k] = w2[k] = 0.f;
+      if (w >= n) continue;
+      const int row = static_cast<int>(w / Hq), h = static_cast<int>(w % Hq);
+      const size_t li = static_cast<size_t>(h) * rows + row;
+      const float l1 = lse_acc[li], l2 = __ldg(lse_part + li);
+      const float M = fmaxf(l1, l2);
+      float L;
+      if (M == NEG_INF) {
+        L = NEG_INF;
+      } else {
+        const float e1 = expf(l1 - M), e2 = expf(l2 - M);
+        const float s = e1 + e2;
+        L = M + logf(s);
+        const float inv = 1.f / s;
+        w1[k] = e1 * inv;
+        w2[k] = e2 * inv;
+      }
+      __syncwarp();
+      if (lane == 0) lse_acc[li] = L;
     }
-    float4* oa = reinterpret_cast<float4*>(o_acc + static_cast<size_t>(w) * d);
-    const float4* op = reinterpret_cast<const float4*>(o_part + static_cast<size_t>(w) * d);
-    for (int c = lane; c < (d >> 2); c += 32) {
-      const float4 x = oa[c], y = __ldg(op + c);
-      oa[c] = make_float4(w1 * x.x + w2 * y.x, w1 * x.y + w2 * y.y, w1 * x.z + w2 * y.z,
-                          w1 * x.w + w2 * y.w);
+    // O rows: all loads first, then the combined writes.
+    for (int c = lane; c < nv; c += 32) {
+      float4 x[MERGE_UNROLL], y[MERGE_UNROLL];
+#pragma unroll
+      for (int k = 0; k < MERGE_UNROLL; ++k) {
+        if (w0 + k >= n) continue;
+        x[k] = reinterpret_cast<const float4*>(o_acc + static_cast<size_t>(w0 + k) * d)[c];
+        y[k] = __ldg(reinterpret_cast<const float4*>(o_part + static_cast<size_t>(w0 + k) * d) + c);
+      }
+#pragma unroll
+      for (int k = 0; k < MERGE_UNROLL; ++k) {
+        if (w0 + k >= n) continue;
+        reinterpret_cast<float4*>(o_acc + static_cast<size_t>(w0 + k) * d)[c] =
+            make_float4(w1[k] * x[k].x + w2[k] * y[k].x, w1[k] * x[k].y + w2[k] * y[k].y,
+                        w1[k] * x[k].z + w2[k] * y[k].z, w1[k] * x[k].w + w2[k] * y[k].w);
+      }
     }
-    __syncwarp();
-    if (lane == 0) lse_acc[li] = L;
   }
 }
 
