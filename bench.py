@@ -58,6 +58,15 @@ def read_peaks():
         return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def fwd_kernel_name(w):
+    """The forward kernel the library runs for a workload: CTA pairs (two query
+    heads of one key/value head per cluster) when d = 128 and Hq / Hkv is even,
+    else one CTA per unit."""
+    if w.d == 128 and (w.Hq // w.Hkv) % 2 == 0:
+        return "attn_tc_pair_kernel<0> (cluster of 2, tcgen05 cta_group::2)"
+    return f"attn_tc_kernel<{w.d},0>"
+
+
 def kernel_traffic():
     """DRAM bytes per launch of the attention kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
@@ -416,7 +425,7 @@ def run_ours(args, world, rank, local):
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "peak_source": f"{peaks['source']} bf16 dense (burst)",
                 "traffic": traffic,
-                "kernel": "attn_tc_kernel<128,0> (+ prep_kernel inside the timed call)",
+                "kernel": fwd_kernel_name(w) + " (+ prep_kernel inside the timed call)",
                 "avg_launch_ms": round(avg_launch_ms, 4),
             },
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
@@ -438,6 +447,8 @@ def kernel_only(args, local):
     import sequence_blockwise_gb300 as sb
     from sequence_blockwise_gb300 import workloads as wl
     w = wl.WORKLOADS[WORKLOAD_INDEX]
+    if args.workload:
+        w = next(x for x in wl.WORKLOADS if x.name == args.workload)
     cu = wl.cu_seqlens(w)
     dev = torch.device("cuda", local)
     q, k, v = wl.make_qkv(w, dev)
@@ -588,6 +599,8 @@ def main():
                     help="per-virtual-rank device time of the chunking policies (one JSON line each)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only W warm-up + K device-resident steps (driver for ncu captures)")
+    ap.add_argument("--workload", default=None,
+                    help="with --kernel-only: workload name (default: the 32K-token layer)")
     args = ap.parse_args()
 
     world, rank, local = dist_setup()

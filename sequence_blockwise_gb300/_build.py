@@ -13,7 +13,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsp_attn.so")
 
-CU_SOURCES = ["sp_api.cu", "attn_tc.cu", "attn_bwd_tc.cu", "attn_simt.cu", "sp_aux.cu"]
+CU_SOURCES = ["sp_api.cu", "attn_tc.cu", "attn_tc_pair.cu", "attn_bwd_tc.cu", "attn_simt.cu", "sp_aux.cu"]
 CPP_SOURCES = ["sp_schedule.cpp"]
 HEADERS = ["sp_internal.h", "sp_device.cuh", "sp_workspace.h", "sp_tiles.cuh"]
 

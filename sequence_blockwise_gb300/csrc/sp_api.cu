@@ -123,10 +123,20 @@ AttnArgs base_args(const void* q, const void* k, const void* v, void* o, float* 
   return a;
 }
 
-sp_status launch_attention(AttnArgs& a, sp_dtype dtype, int sms, cudaStream_t st, int n_units_hint) {
+// heads_full: every item covers all query heads, so units come in pairs of
+// query heads sharing a key/value head whenever Hq / Hkv is even.
+sp_status launch_attention(AttnArgs& a, sp_dtype dtype, int sms, cudaStream_t st, int n_units_hint,
+                           bool heads_full) {
   if (dtype == SP_DTYPE_BF16) {
     if (!encoder()) return SP_ERR_CUDA;
     CUtensorMap mq, mk, mv;
+    if (heads_full && a.d == 128 && (a.Hq / a.Hkv) % 2 == 0) {
+      // CTA pairs: each CTA loads 64 keys of a K tile and 64 dims of a V tile.
+      if (!encode_map(&mq, a.q, a.T, a.Hq, a.d) || !encode_map(&mk, a.k, a.T, a.Hkv, a.d, 64) ||
+          !encode_map(&mv, a.v, a.T, a.Hkv, a.d))
+        return SP_ERR_CUDA;
+      return cuda_fail(sp::launch_attn_tc_pair(a, &mq, &mk, &mv, n_units_hint / 2, st));
+    }
     if (!encode_map(&mq, a.q, a.T, a.Hq, a.d) || !encode_map(&mk, a.k, a.T, a.Hkv, a.d) ||
         !encode_map(&mv, a.v, a.T, a.Hkv, a.d))
       return SP_ERR_CUDA;
@@ -173,7 +183,7 @@ sp_status sp_partial_attn(const void* q, const void* k, const void* v, float* o_
   a.out_mode = 1;
   a.row_base = q_begin;
   a.n_rows = rows;
-  return launch_attention(a, dtype, sms, static_cast<cudaStream_t>(stream), a.inline_n_units);
+  return launch_attention(a, dtype, sms, static_cast<cudaStream_t>(stream), a.inline_n_units, true);
 }
 
 sp_status sp_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
@@ -240,7 +250,7 @@ sp_status sp_packed_attention_ex(const void* q, const void* k, const void* v, vo
   a.out_mode = 0;
   a.row_base = 0;
   a.n_rows = T;
-  return launch_attention(a, dtype, sms, st, 0);
+  return launch_attention(a, dtype, sms, st, 0, item_heads_dev == nullptr);
 }
 
 size_t sp_packed_attention_backward_workspace_size(int64_t n_items, int32_t T, int32_t Hq) {

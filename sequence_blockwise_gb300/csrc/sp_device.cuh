@@ -12,10 +12,14 @@ namespace sp {
 
 // ---------------------------------------------------------------------------
 // Work units. A unit is (group, row group of rows_per_unit rows, query head).
-// Within a group the key/value head varies slowest, then row groups run
-// last-first, and the Hq/Hkv query heads sharing that key/value head are
-// innermost: units running at the same time read the same K/V, which stays in
-// L2.
+// The Hq/Hkv query heads sharing a key/value head are innermost, then row
+// groups run last-first, so that units running at the same time read the same
+// K/V, which stays in L2. When the set-up kernel chose the key/value-head-major
+// layout (header word WS_KV_UNITS > 0: one query head per key/value head, items
+// over all heads), the head varies slowest of all: each head's units of every
+// group (groups in the set-up kernel's order, largest first), then the next
+// head. Otherwise groups follow one another and the key/value head varies
+// slowest within a group.
 
 struct UnitInfo {
   int q0;                 // first row of the unit
@@ -39,17 +43,23 @@ __device__ __forceinline__ const SegEntry& seg_of_unit(const AttnArgs& a, int u)
   return a.segs[lo];
 }
 
-// Units of a group: key/value heads slowest, then row groups from the last,
-// then the group's query heads of that key/value head. Gr = query heads of
-// the range per key/value head (G for a range of whole groups).
+// Within a group's units of one key/value head: row groups from the last, then
+// the group's query heads of that key/value head. Gr = query heads of the
+// range per key/value head (G for a range of whole groups).
 __device__ __forceinline__ UnitInfo unit_info(const AttnArgs& a, int u) {
+  const int kv_units = a.header ? __ldg(a.header + WS_KV_UNITS) : 0;
+  int hk_major = 0;
+  if (kv_units > 0) {  // key/value-head-major layout
+    hk_major = u / kv_units;
+    u -= hk_major * kv_units;
+  }
   const SegEntry& s = seg_of_unit(a, u);
   const int local = u - s.unit_begin;
   const int G = a.Hq / a.Hkv;
   const int Gr = min(G, s.h_hi - s.h_lo);
   const int per_kv = s.n_qgroups * Gr;      // units sharing one key/value head
-  const int hk = local / per_kv;
-  const int rem = local - hk * per_kv;
+  const int hk = kv_units > 0 ? hk_major : local / per_kv;
+  const int rem = kv_units > 0 ? local : local - hk * per_kv;
   const int qg = s.n_qgroups - 1 - rem / Gr;
   UnitInfo ui;
   ui.h = s.h_lo + hk * Gr + rem % Gr;

@@ -30,8 +30,11 @@ static_assert(sizeof(SegEntry) == 32, "SegEntry is 32 bytes");
 // WS_BWD_COUNTER: the backward dK/dV kernel's unit queue.
 // WS_ORDERED: nonzero when some group's items are visited in key order (the
 // set-up kernel's visit order) rather than schedule order.
+// WS_KV_UNITS: units per key/value head when units run key/value-head-major
+// across all groups (Hq == Hkv and every item covers all heads); 0 when they
+// run group by group.
 enum : int { WS_N_SEGS = 0, WS_N_UNITS = 1, WS_STATUS = 2, WS_COUNTER = 3, WS_BWD_COUNTER = 4,
-             WS_ORDERED = 5, WS_HEADER_WORDS = 16 };
+             WS_ORDERED = 5, WS_KV_UNITS = 6, WS_HEADER_WORDS = 16 };
 
 struct AttnArgs {
   const void* q;
@@ -86,6 +89,11 @@ cudaError_t launch_prep(const sp_item* items, const int32_t* item_heads, int64_t
 cudaError_t launch_attn_simt(const AttnArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, const void* tmap_q, const void* tmap_k,
                            const void* tmap_v, int grid, cudaStream_t st);
+// CTA-pair variant (d = 128, Hq / Hkv even, every item over all heads): tmap_k64
+// has a 64-row box. Units 2v and 2v+1 (two query heads of one key/value head,
+// same rows) run on the two CTAs of cluster-pair unit v.
+cudaError_t launch_attn_tc_pair(const AttnArgs& a, const void* tmap_q, const void* tmap_k64,
+                                const void* tmap_v, int n_pairs_hint, cudaStream_t st);
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
                              int32_t rows, int32_t Hq, int32_t d, int grid, cudaStream_t st);
 cudaError_t launch_bwd_rowdot(const void* o, const void* dout, const float* lse, float* ndsc, float* nlse2,
