@@ -621,19 +621,26 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
 template <int D>
 struct QCfg : BCfg<D> {
   using B = BCfg<D>;
-  static constexpr int KSTAGE = 2;
+  // K tile g is read by S(g) and dQ(g), the last MMA of step g; V tile g only
+  // by dP(g), issued a step earlier. So K has one stage more than V: the copy
+  // of step g+3's K starts when dQ(g) is done and has a whole step to land.
+  static constexpr int KSTAGE = 3;
+  static constexpr int VSTAGE = 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = B::TILE;
-  static constexpr int OFF_KV = 2 * B::TILE;  // stage s: K at +0, V at +TILE
-  static constexpr int OFF_BAR = OFF_KV + KSTAGE * 2 * B::TILE;
-  static constexpr int N_BARS = 16;
+  static constexpr int OFF_K = 2 * B::TILE;
+  static constexpr int OFF_V = OFF_K + KSTAGE * B::TILE;
+  static constexpr int OFF_BAR = OFF_V + VSTAGE * B::TILE;
+  static constexpr int N_BARS = 20;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;
 };
 
-enum { QB_Q_FULL = 0, QB_Q_EMPTY = 1, QB_KV_FULL = 2, QB_KV_EMPTY = 4, QB_S_FULL = 6, QB_DP_FULL = 7,
-       QB_S_READ = 8, QB_DS_FULL = 9, QB_ACC_FULL = 10, QB_ACC_EMPTY = 11, QB_DRAIN = 12 };
+// KV_FULL[s] completes when K stage s and the V tile loaded with it have landed.
+enum { QB_Q_FULL = 0, QB_Q_EMPTY = 1, QB_KV_FULL = 2, QB_K_EMPTY = 5, QB_V_EMPTY = 8, QB_S_FULL = 10,
+       QB_DP_FULL = 11, QB_S_READ = 12, QB_DS_FULL = 13, QB_ACC_FULL = 14, QB_ACC_EMPTY = 15,
+       QB_DRAIN = 16 };
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -645,7 +652,9 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sKV = sbase + C::OFF_KV;
+  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO;
+  auto sk = [&](uint32_t g) { return sbase + C::OFF_K + (g % C::KSTAGE) * C::TILE; };
+  auto sv = [&](uint32_t g) { return sbase + C::OFF_V + (g % C::VSTAGE) * C::TILE; };
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -658,8 +667,9 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     mbar_init(bar(QB_Q_EMPTY), 1);
     for (int s = 0; s < C::KSTAGE; ++s) {
       mbar_init(bar(QB_KV_FULL + s), 1);
-      mbar_init(bar(QB_KV_EMPTY + s), 1);
+      mbar_init(bar(QB_K_EMPTY + s), 1);
     }
+    for (int s = 0; s < C::VSTAGE; ++s) mbar_init(bar(QB_V_EMPTY + s), 1);
     mbar_init(bar(QB_S_FULL), 1);
     mbar_init(bar(QB_DP_FULL), 1);
     mbar_init(bar(QB_S_READ), 8);   // both compute warpgroups, one arrival per warp
@@ -693,8 +703,8 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t kv_cnt = 0, unit_cnt = 0;
-      int armed_q = 0, armed_kv[C::KSTAGE] = {0, 0};
-      uint32_t par_q = 0, par_kv[C::KSTAGE] = {0, 0};
+      int armed_q = 0, armed_kv[C::KSTAGE] = {};
+      uint32_t par_q = 0, par_kv[C::KSTAGE] = {};
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
         const UnitInfo ui = unit_info(f, u);
@@ -710,15 +720,15 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         Cursor cur = make_cursor(f, ui, qt, f.causal);
         int ka, kb, cls[2];
         while (next_tile(f, cur, qt, ka, kb, cls)) {
-          const int st = kv_cnt % C::KSTAGE;
-          const uint32_t ph = (kv_cnt / C::KSTAGE) & 1;
-          if (!mbar_wait_bounded(bar(QB_KV_EMPTY + st), ph ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
+          const int st = kv_cnt % C::KSTAGE, vs = kv_cnt % C::VSTAGE;
+          const uint32_t ph = (kv_cnt / C::KSTAGE) & 1, vph = (kv_cnt / C::VSTAGE) & 1;
+          if (!mbar_wait_bounded(bar(QB_K_EMPTY + st), ph ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_bounded(bar(QB_V_EMPTY + vs), vph ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(QB_KV_FULL + st), 2 * C::TILE);
           armed_kv[st] = 1;
           par_kv[st] = ph;
-          const uint32_t skv = sKV + st * 2 * C::TILE;
-          load_rows128<D>(skv, &tmk, bar(QB_KV_FULL + st), hk, ka, f.T);
-          load_rows128<D>(skv + C::TILE, &tmv, bar(QB_KV_FULL + st), hk, ka, f.T);
+          load_rows128<D>(sk(kv_cnt), &tmk, bar(QB_KV_FULL + st), hk, ka, f.T);
+          load_rows128<D>(sv(kv_cnt), &tmv, bar(QB_KV_FULL + st), hk, ka, f.T);
           ++kv_cnt;
         }
       }
@@ -753,11 +763,11 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
           if (!mbar_wait_bounded(bar(QB_KV_FULL + g % C::KSTAGE), (g / C::KSTAGE) & 1, tmo, f.err,
                                  abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t skv = sKV + (g % C::KSTAGE) * 2 * C::TILE;
-          mma_s<D>(tS, sQ, skv);               // S = Q K^T
+          mma_s<D>(tS, sQ, sk(g));          // S = Q K^T
           tc_commit(bar(QB_S_FULL));
-          mma_s<D>(tdP, sDO, skv + C::TILE);   // dP = dO V^T
+          mma_s<D>(tdP, sDO, sv(g));        // dP = dO V^T
           tc_commit(bar(QB_DP_FULL));
+          tc_commit(bar(QB_V_EMPTY + g % C::VSTAGE));
         }
         if (unit_cnt > 0 &&
             !mbar_wait_bounded(bar(QB_ACC_EMPTY), (unit_cnt - 1) & 1, tmo, f.err, abort_flag)) { ok = false; break; }
@@ -765,24 +775,23 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
           const uint32_t g = kv_cnt + n;
           const uint32_t ph = g & 1;
           const bool more = n + 1 < nblk;
-          const uint32_t skv = sKV + (g % C::KSTAGE) * 2 * C::TILE;
-          const uint32_t skv1 = sKV + ((g + 1) % C::KSTAGE) * 2 * C::TILE;
           if (more) {
             // Both warpgroups have read S(g): S may be overwritten.
             if (!mbar_wait_bounded(bar(QB_S_READ), ph, tmo, f.err, abort_flag)) { ok = false; break; }
             if (!mbar_wait_bounded(bar(QB_KV_FULL + (g + 1) % C::KSTAGE), ((g + 1) / C::KSTAGE) & 1, tmo,
                                    f.err, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            mma_s<D>(tS, sQ, skv1);
+            mma_s<D>(tS, sQ, sk(g + 1));
             tc_commit(bar(QB_S_FULL));
           }
           if (!mbar_wait_bounded(bar(QB_DS_FULL), ph, tmo, f.err, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          mma_acc<D>(tdQ, tdP, skv, n > 0);  // dQ += dS K
-          tc_commit(bar(QB_KV_EMPTY + g % C::KSTAGE));
+          mma_acc<D>(tdQ, tdP, sk(g), n > 0);  // dQ += dS K
+          tc_commit(bar(QB_K_EMPTY + g % C::KSTAGE));
           if (more) {
-            mma_s<D>(tdP, sDO, skv1 + C::TILE);
+            mma_s<D>(tdP, sDO, sv(g + 1));
             tc_commit(bar(QB_DP_FULL));
+            tc_commit(bar(QB_V_EMPTY + (g + 1) % C::VSTAGE));
           }
         }
         if (!ok) break;
