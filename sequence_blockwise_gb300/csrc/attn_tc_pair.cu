@@ -16,8 +16,9 @@
 // kernel (shared-memory bandwidth shared by the tensor core and TMA).
 //
 // Roles (12 warps per CTA):
-//   warp 0      TMA producer, in both CTAs: Q tiles of the CTA's head, and
-//               the CTA's halves of K (3 stages) and V (4 stages). Copies are
+//   warp 0      TMA producer, in both CTAs: Q tiles of the CTA's head (two
+//               buffers: the next unit's Q loads during the current unit), and
+//               the CTA's halves of K (2 stages) and V (3 stages). Copies are
 //               counted on the first CTA's barriers. The first CTA's producer
 //               also claims the work and passes it to both CTAs.
 //   warp 1      allocates tensor memory (both CTAs); in the first CTA, lane 0
@@ -38,15 +39,19 @@ constexpr int REC_TILE = 16, REC_LAST = 32;
 
 struct PCfg {
   static constexpr int D = 128;
-  static constexpr int KSTAGE = 3;
-  static constexpr int VSTAGE = 4;
+  // Two Q buffers (the next unit's Q tiles load while the current unit runs),
+  // two K and three V stages (V is held one MMA group longer than K).
+  static constexpr int QBUF = 2;
+  static constexpr int KSTAGE = 2;
+  static constexpr int VSTAGE = 3;
   static constexpr int Q_SUB = 128 * 128;           // [128 rows][64 dims] bf16
   static constexpr int Q_TILE = 2 * Q_SUB;          // 128 rows x 128 dims
   static constexpr int K_SUB = 64 * 128;            // [64 keys][64 dims]
   static constexpr int K_STAGE_BYTES = 2 * K_SUB;   // half a K tile: 64 keys x 128 dims
   static constexpr int V_STAGE_BYTES = 128 * 128;   // half a V tile: 128 keys x 64 dims
+  static constexpr int Q_BUF_BYTES = 2 * Q_TILE;   // the unit's two Q tiles
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
+  static constexpr int OFF_K = OFF_Q + QBUF * Q_BUF_BYTES;
   static constexpr int OFF_V = OFF_K + KSTAGE * K_STAGE_BYTES;
   static constexpr int OFF_BAR = OFF_V + VSTAGE * V_STAGE_BYTES;
   static constexpr int N_BARS = 24;
@@ -66,9 +71,9 @@ struct PCfg {
 
 // Barrier slots. The full barriers (Q_FULL, KV_FULL), P_FULL and U_EMPTY are
 // used in the first CTA only; the others exist in both CTAs and receive the
-// MMA lane's multicast commits.
+// MMA lane's multicast commits. Q_FULL / Q_EMPTY: one per Q buffer.
 enum {
-  B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_K_EMPTY = 5, B_V_EMPTY = 8,
+  B_Q_FULL = 0, B_Q_EMPTY = 2, B_KV_FULL = 4, B_K_EMPTY = 6, B_V_EMPTY = 8,
   B_S_FULL = 12, B_P_FULL = 14, B_O_FULL = 16, B_DRAIN = 18, B_U_FULL = 19, B_U_EMPTY = 21
 };
 static_assert(B_U_EMPTY + 2 <= PCfg::N_BARS, "barrier slots");
@@ -270,8 +275,10 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const bool lead = rank == 0;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_Q_FULL), 1);
-    mbar_init(bar(B_Q_EMPTY), 1);
+    for (int b = 0; b < C::QBUF; ++b) {
+      mbar_init(bar(B_Q_FULL + b), 1);
+      mbar_init(bar(B_Q_EMPTY + b), 1);
+    }
     for (int s = 0; s < C::KSTAGE; ++s) {
       mbar_init(bar(B_KV_FULL + s), 1);
       mbar_init(bar(B_K_EMPTY + s), 1);
@@ -321,8 +328,8 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       uint32_t kph = 0, vph = 0;
       int armed_k[C::KSTAGE] = {};
       uint32_t par_k[C::KSTAGE] = {};
-      int armed_q = 0;
-      uint32_t par_q = 0;
+      int armed_q[C::QBUF] = {};
+      uint32_t par_q[C::QBUF] = {};
       bool ok = true;
       int k_static = 0;
       auto fetch = [&]() -> int {
@@ -360,16 +367,18 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         const UnitInfo ui = unit_info(a, 2 * v + static_cast<int>(rank));
         const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
         const int hk = ui.h / G;
-        if (!mbar_wait_bounded(bar(B_Q_EMPTY), (unit_cnt & 1) ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
+        const int qb = unit_cnt & 1;
+        const uint32_t qph = (unit_cnt >> 1) & 1;
+        if (!mbar_wait_bounded(bar(B_Q_EMPTY + qb), qph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
         if (lead) {
-          mbar_arrive_expect_tx(bar(B_Q_FULL), C::Q_TX);
-          armed_q = 1;
-          par_q = unit_cnt & 1;
+          mbar_arrive_expect_tx(bar(B_Q_FULL + qb), C::Q_TX);
+          armed_q[qb] = 1;
+          par_q[qb] = qph;
         }
         for (int i = 0; i < 2; ++i)
           for (int s = 0; s < 2; ++s)
-            tma_load_3d_pair(sQ + i * C::Q_TILE + s * C::Q_SUB, &tmq, lbar(B_Q_FULL), 64 * s, ui.h,
-                             ui.q0 + 128 * i);
+            tma_load_3d_pair(sQ + qb * C::Q_BUF_BYTES + i * C::Q_TILE + s * C::Q_SUB, &tmq,
+                             lbar(B_Q_FULL + qb), 64 * s, ui.h, ui.q0 + 128 * i);
         Cursor cur = make_cursor(a, ui, qt, a.causal);
         int ka = 0, kb = 0, cls[2] = {0, 0};
         bool have = next_tile(a, cur, qt, ka, kb, cls);
@@ -416,7 +425,8 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         volatile int no_abort = 0;
         const unsigned long long drain = 50000000ull;
         if (lead) {
-          if (armed_q) mbar_wait_bounded(bar(B_Q_FULL), par_q, drain, a.err, &no_abort);
+          for (int b = 0; b < C::QBUF; ++b)
+            if (armed_q[b]) mbar_wait_bounded(bar(B_Q_FULL + b), par_q[b], drain, a.err, &no_abort);
           for (int s = 0; s < C::KSTAGE; ++s)
             if (armed_k[s]) mbar_wait_bounded(bar(B_KV_FULL + s), par_k[s], drain, a.err, &no_abort);
         } else {
@@ -430,8 +440,8 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (first CTA)
     if (lead && lane == 0) {
-      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
-      const uint64_t dq1 = smem_desc_sw128(sQ + C::Q_TILE, 16, 1024);
+      const uint64_t dq00 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dq01 = smem_desc_sw128(sQ + C::Q_TILE, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sV, C::V_STAGE_BYTES, 1024);
       uint32_t unit_cnt = 0, pcnt0 = 0, pcnt1 = 0;
@@ -454,8 +464,11 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         mbar_arrive(bar(B_U_EMPTY + uslot));
         if (++uslot == 2) { uslot = 0; uph ^= 1; }
         if (v < 0) break;
-        if (!mbar_wait_bounded(bar(B_Q_FULL), unit_cnt & 1, tmo, a.err, abort_flag)) { ok = false; break; }
+        const int qb = unit_cnt & 1;
+        if (!mbar_wait_bounded(bar(B_Q_FULL + qb), (unit_cnt >> 1) & 1, tmo, a.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
+        const uint64_t qoff = static_cast<uint64_t>((qb * C::Q_BUF_BYTES) >> 4);
+        const uint64_t dq0 = dq00 + qoff, dq1 = dq01 + qoff;
         int has_pv0 = 0, has_pv1 = 0;
         int have_prev = 0, prev_vs = 0, prev_c1 = 0;
         while (true) {
@@ -525,7 +538,7 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           }
           commit_both(bar(B_V_EMPTY + prev_vs));
         }
-        commit_both(bar(B_Q_EMPTY));
+        commit_both(bar(B_Q_EMPTY + qb));
         commit_both(bar(B_O_FULL + 0));
         commit_both(bar(B_O_FULL + 1));
       }
