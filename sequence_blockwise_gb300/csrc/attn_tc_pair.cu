@@ -57,8 +57,8 @@ struct PCfg {
   static constexpr int N_BARS = 24;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;   // TMEM address, abort flag
   static constexpr int OFF_REC = OFF_MISC + 8;
-  static constexpr int OFF_URING = OFF_REC + 4 * KSTAGE;
-  static constexpr int SMEM_ALLOC = OFF_URING + 8 + 1024;
+  static constexpr int OFF_URING = (OFF_REC + 4 * KSTAGE + 15) & ~15;  // two unit records
+  static constexpr int SMEM_ALLOC = OFF_URING + 2 * 128 + 1024;
   static constexpr int TM_S = 0;
   static constexpr int TM_O = 256;
   static constexpr int TMEM_COLS = 512;
@@ -77,6 +77,61 @@ enum {
   B_S_FULL = 12, B_P_FULL = 14, B_O_FULL = 16, B_DRAIN = 18, B_U_FULL = 19, B_U_EMPTY = 21
 };
 static_assert(B_U_EMPTY + 2 <= PCfg::N_BARS, "barrier slots");
+
+// A unit slot holds the unit's record: everything the roles need to walk it,
+// computed once by the first CTA's producer (one unit ahead of the others) and
+// stored into both CTAs' slot. Both CTAs' units have the same rows, documents
+// and items; the second CTA's query head is the first's plus one.
+constexpr int UREC_WORDS = 32;  // slot stride (int32 words)
+enum { UR_V = 0, UR_H = 1, UR_Q0 = 2, UR_QT = 3, UR_CUR = 13, UR_N = 17 };
+
+__device__ __forceinline__ void urec_pack(int v, const UnitInfo& ui, const QTile (&qt)[2], const Cursor& cur,
+                                          int (&w)[UR_N]) {
+  w[UR_V] = v;
+  w[UR_H] = ui.h;
+  w[UR_Q0] = ui.q0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    w[UR_QT + 5 * i + 0] = qt[i].qa;
+    w[UR_QT + 5 * i + 1] = qt[i].qb;
+    w[UR_QT + 5 * i + 2] = qt[i].ds;
+    w[UR_QT + 5 * i + 3] = qt[i].de;
+    w[UR_QT + 5 * i + 4] = qt[i].one_doc;
+  }
+  w[UR_CUR + 0] = cur.item;
+  w[UR_CUR + 1] = cur.item_end;
+  w[UR_CUR + 2] = cur.lo;
+  w[UR_CUR + 3] = cur.hi;
+}
+
+// Reads a record (v >= 0) into the head of the reading CTA (rank), the unit's
+// first row, its Q tiles and a fresh cursor.
+__device__ __forceinline__ void urec_read(const volatile int* rs, uint32_t rank, int& h, int& q0,
+                                          QTile (&qt)[2], Cursor& cur) {
+  h = rs[UR_H] + static_cast<int>(rank);
+  q0 = rs[UR_Q0];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    qt[i].qa = rs[UR_QT + 5 * i + 0];
+    qt[i].qb = rs[UR_QT + 5 * i + 1];
+    qt[i].ds = rs[UR_QT + 5 * i + 2];
+    qt[i].de = rs[UR_QT + 5 * i + 3];
+    qt[i].one_doc = rs[UR_QT + 5 * i + 4];
+  }
+  cur.item = rs[UR_CUR + 0];
+  cur.item_end = rs[UR_CUR + 1];
+  cur.kv_e = 0;
+  cur.k0 = 0;
+  cur.lo = rs[UR_CUR + 2];
+  cur.hi = rs[UR_CUR + 3];
+}
+
+// 32-byte global store.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                  "r"(w[7]) : "memory");
+}
 
 // Consumers of a unit slot: the MMA lane and 8 softmax warps of the first CTA,
 // the producer and 8 softmax warps of the second.
@@ -348,25 +403,42 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       uint32_t uph = 0;
       int v_next = lead ? fetch() : -1;
       for (;; ++unit_cnt) {
-        int v;
+        int v, h = 0, q0 = 0;
+        QTile qt[2];
+        Cursor cur;
+        volatile int* rs = uring + UREC_WORDS * uslot;
         if (lead) {
           v = v_next;
+          int w[UR_N];
+          w[UR_V] = v;
+          if (v >= 0) {
+            const UnitInfo ui = unit_info(a, 2 * v);
+            qt[0] = make_qtile(a, ui, 0);
+            qt[1] = make_qtile(a, ui, 1);
+            cur = make_cursor(a, ui, qt, a.causal);
+            h = ui.h;
+            q0 = ui.q0;
+            urec_pack(v, ui, qt, cur, w);
+          }
           if (!wait_cl(bar(B_U_EMPTY + uslot), uph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
-          uring[uslot] = v;
-          st_cluster(peer_uring + 4u * uslot, v);
+          const int n = v >= 0 ? static_cast<int>(UR_N) : 1;
+          const uint32_t prs = peer_uring + 4u * UREC_WORDS * uslot;
+          for (int i = 0; i < n; ++i) {
+            rs[i] = w[i];
+            st_cluster(prs + 4u * i, w[i]);
+          }
           mbar_arrive(bar(B_U_FULL + uslot));
           arrive_cluster(peer_ufull + 8u * uslot);
         } else {
           if (!wait_cl(bar(B_U_FULL + uslot), uph, tmo, a.err, abort_flag)) { ok = false; break; }
-          v = uring[uslot];
+          v = rs[UR_V];
+          if (v >= 0) urec_read(rs, rank, h, q0, qt, cur);
           arrive_cluster(lbar(B_U_EMPTY + uslot));
         }
         if (++uslot == 2) { uslot = 0; uph ^= 1; }
         if (v < 0) break;
         if (lead) v_next = fetch();
-        const UnitInfo ui = unit_info(a, 2 * v + static_cast<int>(rank));
-        const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
-        const int hk = ui.h / G;
+        const int hk = h / G;
         const int qb = unit_cnt & 1;
         const uint32_t qph = (unit_cnt >> 1) & 1;
         if (!mbar_wait_bounded(bar(B_Q_EMPTY + qb), qph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
@@ -378,8 +450,7 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         for (int i = 0; i < 2; ++i)
           for (int s = 0; s < 2; ++s)
             tma_load_3d_pair(sQ + qb * C::Q_BUF_BYTES + i * C::Q_TILE + s * C::Q_SUB, &tmq,
-                             lbar(B_Q_FULL + qb), 64 * s, ui.h, ui.q0 + 128 * i);
-        Cursor cur = make_cursor(a, ui, qt, a.causal);
+                             lbar(B_Q_FULL + qb), 64 * s, h, q0 + 128 * i);
         int ka = 0, kb = 0, cls[2] = {0, 0};
         bool have = next_tile(a, cur, qt, ka, kb, cls);
         if (!have) {
@@ -460,7 +531,7 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       uint32_t uph = 0;
       for (;; ++unit_cnt) {
         if (!wait_cl(bar(B_U_FULL + uslot), uph, tmo, a.err, abort_flag)) { ok = false; break; }
-        const int v = uring[uslot];
+        const int v = uring[UREC_WORDS * uslot + UR_V];
         mbar_arrive(bar(B_U_EMPTY + uslot));
         if (++uslot == 2) { uslot = 0; uph ^= 1; }
         if (v < 0) break;
@@ -560,32 +631,41 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     const float sl2 = a.scale_log2;
     const float NEG_INF = -__int_as_float(0x7f800000);
     const uint32_t p_full = lbar(B_P_FULL + wg);
+    // O rows start 32-byte aligned when the output does (rows are 256 or 512 bytes).
+    const bool o_a32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
     uint32_t s_cnt = 0, unit_cnt = 0;
     bool ok = true;
     int uslot = 0;
     uint32_t uph = 0;
     for (;; ++unit_cnt) {
       if (!wait_cl(bar(B_U_FULL + uslot), uph, tmo, a.err, abort_flag)) { ok = false; break; }
-      const int v = uring[uslot];
+      const volatile int* rs = uring + UREC_WORDS * uslot;
+      const int v = rs[UR_V];
+      int h = 0, q0 = 0;
+      QTile qt[2];
+      Cursor cur;
+      if (v >= 0) urec_read(rs, rank, h, q0, qt, cur);
       __syncwarp();
       if (lane == 0) arrive_cluster(lbar(B_U_EMPTY + uslot));
       if (++uslot == 2) { uslot = 0; uph ^= 1; }
       if (v < 0) break;
-      const UnitInfo ui = unit_info(a, 2 * v + static_cast<int>(rank));
-      const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
       const QTile my = wg ? qt[1] : qt[0];
-      const int t = ui.q0 + 128 * wg + r;
+      const int t = q0 + 128 * wg + r;
       const bool valid = (t >= my.qa) && (t < my.qb);
       int rds = 0, rde = 0;
       if (valid) {
-        const int dd = doc_of(a.cu, a.ndocs, t);
-        rds = __ldg(a.cu + dd);
-        rde = __ldg(a.cu + dd + 1);
+        if (my.one_doc) {  // the tile's rows are all in one document
+          rds = my.ds;
+          rde = my.de;
+        } else {
+          const int dd = doc_of(a.cu, a.ndocs, t);
+          rds = __ldg(a.cu + dd);
+          rde = __ldg(a.cu + dd + 1);
+        }
       }
       const int rcausal_end = a.causal ? t + 1 : 0x7fffffff;
       float m = NEG_INF, l = 0.f;
       int has_pv = 0;
-      Cursor cur = make_cursor(a, ui, qt, a.causal);
       int ka, kb, cls[2];
       while (next_tile(a, cur, qt, ka, kb, cls)) {
         const int c = wg ? cls[1] : cls[0];
@@ -686,33 +766,54 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         if (valid) {
           if (OUT_FP32) {
             float* dst = static_cast<float*>(a.o) +
-                         (static_cast<size_t>(t - a.row_base) * a.Hq + ui.h) * D + 32 * ch;
+                         (static_cast<size_t>(t - a.row_base) * a.Hq + h) * D + 32 * ch;
+            if (o_a32) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              float4 v4 = make_float4(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv,
-                                      __uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
-              *reinterpret_cast<float4*>(dst + j) = v4;
+              for (int j = 0; j < 32; j += 8) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(rr[j + e]) * inv);
+                st_global_v8(dst + j, w);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4) {
+                float4 v4 = make_float4(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv,
+                                        __uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
+                *reinterpret_cast<float4*>(dst + j) = v4;
+              }
             }
           } else {
             uint16_t* dst = static_cast<uint16_t*>(a.o) +
-                            (static_cast<size_t>(t) * a.Hq + ui.h) * D + 32 * ch;
+                            (static_cast<size_t>(t) * a.Hq + h) * D + 32 * ch;
+            if (o_a32) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(rr[j + 4]) * inv, __uint_as_float(rr[j + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(rr[j + 6]) * inv, __uint_as_float(rr[j + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + j) = w;
+              for (int j = 0; j < 32; j += 16) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  w[e] = pack_bf16x2(__uint_as_float(rr[j + 2 * e]) * inv, __uint_as_float(rr[j + 2 * e + 1]) * inv);
+                st_global_v8(dst + j, w);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv);
+                w.y = pack_bf16x2(__uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
+                w.z = pack_bf16x2(__uint_as_float(rr[j + 4]) * inv, __uint_as_float(rr[j + 5]) * inv);
+                w.w = pack_bf16x2(__uint_as_float(rr[j + 6]) * inv, __uint_as_float(rr[j + 7]) * inv);
+                *reinterpret_cast<uint4*>(dst + j) = w;
+              }
             }
           }
         }
       }
       if (valid) {
         if (OUT_FP32)
-          a.lse[static_cast<size_t>(ui.h) * a.n_rows + (t - a.row_base)] = lse_v;
+          a.lse[static_cast<size_t>(h) * a.n_rows + (t - a.row_base)] = lse_v;
         else
-          a.lse[static_cast<size_t>(ui.h) * a.T + t] = lse_v;
+          a.lse[static_cast<size_t>(h) * a.T + t] = lse_v;
       }
       tc_fence_before();
     }
