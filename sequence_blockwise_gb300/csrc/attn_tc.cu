@@ -368,6 +368,9 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           if (r & REC_LAST) break;
         }
         if (!ok) break;
+        // O_0 is complete once the PV0 issued so far are: the softmax warps of Q
+        // tile 0 may read it out while the last PV1 still waits for its P.
+        tc_commit(bar(B_O_FULL + 0));
         if (have_prev) {
           if (prev_c1 != CLS_SKIP) {
             const uint64_t bVp = dv0 + static_cast<uint64_t>(prev_vs) * kstep;
@@ -380,7 +383,6 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           tc_commit(bar(B_V_EMPTY + prev_vs));
         }
         tc_commit(bar(B_Q_EMPTY));
-        tc_commit(bar(B_O_FULL + 0));
         tc_commit(bar(B_O_FULL + 1));
       }
       // Every MMA issued has completed before tensor memory is released.

@@ -598,6 +598,9 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           if (r & REC_LAST) break;
         }
         if (!ok) break;
+        // O_0 is complete once the PV0 issued so far are: the softmax warps of Q
+        // tile 0 may read it out while the last PV1 still waits for its P.
+        commit_both(bar(B_O_FULL + 0));
         if (have_prev) {
           if (prev_c1 != CLS_SKIP) {
             const uint64_t bVp = dv0 + static_cast<uint64_t>(prev_vs) * vstep;
@@ -610,7 +613,6 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           commit_both(bar(B_V_EMPTY + prev_vs));
         }
         commit_both(bar(B_Q_EMPTY + qb));
-        commit_both(bar(B_O_FULL + 0));
         commit_both(bar(B_O_FULL + 1));
       }
       // Every MMA issued has completed before tensor memory is released.
