@@ -19,10 +19,12 @@
 //   warp 0      TMA producer, in both CTAs: Q tiles of the CTA's head (two
 //               buffers: the next unit's Q loads during the current unit), and
 //               the CTA's halves of K (2 stages) and V (3 stages). Copies are
-//               counted on the first CTA's barriers. The first CTA's producer
-//               also claims the work and passes it to both CTAs.
+//               counted on the first CTA's barriers.
 //   warp 1      allocates tensor memory (both CTAs); in the first CTA, lane 0
 //               issues every MMA of the pair and signals both CTAs.
+//   warp 2      in the first CTA, lane 0 claims the work units and publishes
+//               each unit's record (rows, Q tiles, documents, the cursor on
+//               its first tile) to both CTAs, up to two units ahead.
 //   warps 4-11  softmax for Q tile 0 / 1 of the CTA's head, as in attn_tc.cu.
 // Tensor memory per CTA: S_i at 128 i, P_i in columns [64, 128) of S_i, O_i at
 // 256 + 128 i. The MMA order per tile is QK0(j), PV1(j-1), QK1(j), PV0(j).
@@ -83,8 +85,11 @@ static_assert(B_U_EMPTY + 2 <= PCfg::N_BARS, "barrier slots");
 // stored into both CTAs' slot. Both CTAs' units have the same rows, documents
 // and items; the second CTA's query head is the first's plus one.
 constexpr int UREC_WORDS = 32;  // slot stride (int32 words)
-enum { UR_V = 0, UR_H = 1, UR_Q0 = 2, UR_QT = 3, UR_CUR = 13, UR_N = 17 };
+enum { UR_V = 0, UR_H = 1, UR_Q0 = 2, UR_QT = 3, UR_CUR = 13, UR_N = 19 };
 
+// The record's cursor stands on the unit's first tile (the producer has
+// walked to it), so a reader's first next_tile returns it without reading
+// any item.
 __device__ __forceinline__ void urec_pack(int v, const UnitInfo& ui, const QTile (&qt)[2], const Cursor& cur,
                                           int (&w)[UR_N]) {
   w[UR_V] = v;
@@ -100,12 +105,14 @@ __device__ __forceinline__ void urec_pack(int v, const UnitInfo& ui, const QTile
   }
   w[UR_CUR + 0] = cur.item;
   w[UR_CUR + 1] = cur.item_end;
-  w[UR_CUR + 2] = cur.lo;
-  w[UR_CUR + 3] = cur.hi;
+  w[UR_CUR + 2] = cur.kv_e;
+  w[UR_CUR + 3] = cur.k0;
+  w[UR_CUR + 4] = cur.lo;
+  w[UR_CUR + 5] = cur.hi;
 }
 
 // Reads a record (v >= 0) into the head of the reading CTA (rank), the unit's
-// first row, its Q tiles and a fresh cursor.
+// first row, its Q tiles and the cursor.
 __device__ __forceinline__ void urec_read(const volatile int* rs, uint32_t rank, int& h, int& q0,
                                           QTile (&qt)[2], Cursor& cur) {
   h = rs[UR_H] + static_cast<int>(rank);
@@ -120,10 +127,10 @@ __device__ __forceinline__ void urec_read(const volatile int* rs, uint32_t rank,
   }
   cur.item = rs[UR_CUR + 0];
   cur.item_end = rs[UR_CUR + 1];
-  cur.kv_e = 0;
-  cur.k0 = 0;
-  cur.lo = rs[UR_CUR + 2];
-  cur.hi = rs[UR_CUR + 3];
+  cur.kv_e = rs[UR_CUR + 2];
+  cur.k0 = rs[UR_CUR + 3];
+  cur.lo = rs[UR_CUR + 4];
+  cur.hi = rs[UR_CUR + 5];
 }
 
 // 32-byte global store.
@@ -133,9 +140,9 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
                   "r"(w[7]) : "memory");
 }
 
-// Consumers of a unit slot: the MMA lane and 8 softmax warps of the first CTA,
-// the producer and 8 softmax warps of the second.
-constexpr int UNIT_CONSUMERS = 18;
+// Consumers of a unit slot: the producer, the MMA lane and 8 softmax warps of
+// the first CTA, the producer and 8 softmax warps of the second.
+constexpr int UNIT_CONSUMERS = 19;
 // Softmax warps of both CTAs storing P_i.
 constexpr int P_ARRIVALS = 8;
 
@@ -386,58 +393,22 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       int armed_q[C::QBUF] = {};
       uint32_t par_q[C::QBUF] = {};
       bool ok = true;
-      int k_static = 0;
-      auto fetch = [&]() -> int {
-        int v;
-        if (a.work_counter) {
-          v = atomicAdd(a.work_counter, 1);
-        } else {
-          v = static_cast<int>(cluster_idx()) + k_static * static_cast<int>(n_clusters());
-          ++k_static;
-        }
-        return v < n_pairs ? v : -1;
-      };
-      const uint32_t peer_uring = map_to(smem_u32(const_cast<int*>(uring)), 1);
-      const uint32_t peer_ufull = map_to(bar(B_U_FULL), 1);
       int uslot = 0;
       uint32_t uph = 0;
-      int v_next = lead ? fetch() : -1;
       for (;; ++unit_cnt) {
-        int v, h = 0, q0 = 0;
+        int h = 0, q0 = 0;
         QTile qt[2];
         Cursor cur;
-        volatile int* rs = uring + UREC_WORDS * uslot;
-        if (lead) {
-          v = v_next;
-          int w[UR_N];
-          w[UR_V] = v;
-          if (v >= 0) {
-            const UnitInfo ui = unit_info(a, 2 * v);
-            qt[0] = make_qtile(a, ui, 0);
-            qt[1] = make_qtile(a, ui, 1);
-            cur = make_cursor(a, ui, qt, a.causal);
-            h = ui.h;
-            q0 = ui.q0;
-            urec_pack(v, ui, qt, cur, w);
-          }
-          if (!wait_cl(bar(B_U_EMPTY + uslot), uph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
-          const int n = v >= 0 ? static_cast<int>(UR_N) : 1;
-          const uint32_t prs = peer_uring + 4u * UREC_WORDS * uslot;
-          for (int i = 0; i < n; ++i) {
-            rs[i] = w[i];
-            st_cluster(prs + 4u * i, w[i]);
-          }
-          mbar_arrive(bar(B_U_FULL + uslot));
-          arrive_cluster(peer_ufull + 8u * uslot);
-        } else {
-          if (!wait_cl(bar(B_U_FULL + uslot), uph, tmo, a.err, abort_flag)) { ok = false; break; }
-          v = rs[UR_V];
-          if (v >= 0) urec_read(rs, rank, h, q0, qt, cur);
-          arrive_cluster(lbar(B_U_EMPTY + uslot));
-        }
+        bool have = false;
+        int ka = 0, kb = 0, cls[2] = {0, 0};
+        const volatile int* rs = uring + UREC_WORDS * uslot;
+        if (!wait_cl(bar(B_U_FULL + uslot), uph, tmo, a.err, abort_flag)) { ok = false; break; }
+        const int v = rs[UR_V];
+        if (v >= 0) urec_read(rs, rank, h, q0, qt, cur);
+        arrive_cluster(lbar(B_U_EMPTY + uslot));
         if (++uslot == 2) { uslot = 0; uph ^= 1; }
         if (v < 0) break;
-        if (lead) v_next = fetch();
+        have = next_tile(a, cur, qt, ka, kb, cls);
         const int hk = h / G;
         const int qb = unit_cnt & 1;
         const uint32_t qph = (unit_cnt >> 1) & 1;
@@ -451,8 +422,6 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           for (int s = 0; s < 2; ++s)
             tma_load_3d_pair(sQ + qb * C::Q_BUF_BYTES + i * C::Q_TILE + s * C::Q_SUB, &tmq,
                              lbar(B_Q_FULL + qb), 64 * s, h, q0 + 128 * i);
-        int ka = 0, kb = 0, cls[2] = {0, 0};
-        bool have = next_tile(a, cur, qt, ka, kb, cls);
         if (!have) {
           if (!mbar_wait_bounded(bar(B_K_EMPTY + kst), kph ^ 1, tmo, a.err, abort_flag)) { ok = false; break; }
           if (lead) {
@@ -505,6 +474,53 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           while (globaltimer_ns() - t0 < drain) {
           }
         }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ unit scheduler (first CTA)
+    if (lead && lane == 0) {
+      int k_static = 0;
+      auto fetch = [&]() -> int {
+        int v;
+        if (a.work_counter) {
+          v = atomicAdd(a.work_counter, 1);
+        } else {
+          v = static_cast<int>(cluster_idx()) + k_static * static_cast<int>(n_clusters());
+          ++k_static;
+        }
+        return v < n_pairs ? v : -1;
+      };
+      const uint32_t peer_uring = map_to(smem_u32(const_cast<int*>(uring)), 1);
+      const uint32_t peer_ufull = map_to(bar(B_U_FULL), 1);
+      int uslot = 0;
+      uint32_t uph = 0;
+      for (;;) {
+        // The record is built before the slot is free: its table searches and
+        // the walk to the first tile overlap the other roles' work.
+        const int v = fetch();
+        int w[UR_N];
+        w[UR_V] = v;
+        if (v >= 0) {
+          const UnitInfo ui = unit_info(a, 2 * v);
+          QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
+          Cursor cur = make_cursor(a, ui, qt, a.causal);
+          int ka = 0, kb = 0, cls[2];
+          if (next_tile(a, cur, qt, ka, kb, cls)) cur.k0 = ka;  // back onto the first tile
+          urec_pack(v, ui, qt, cur, w);
+        }
+        if (!wait_cl(bar(B_U_EMPTY + uslot), uph ^ 1, tmo, a.err, abort_flag)) break;
+        volatile int* rs = uring + UREC_WORDS * uslot;
+        const int n = v >= 0 ? static_cast<int>(UR_N) : 1;
+        const uint32_t prs = peer_uring + 4u * UREC_WORDS * uslot;
+        for (int i = 0; i < n; ++i) {
+          rs[i] = w[i];
+          st_cluster(prs + 4u * i, w[i]);
+        }
+        mbar_arrive(bar(B_U_FULL + uslot));
+        arrive_cluster(peer_ufull + 8u * uslot);
+        if (++uslot == 2) { uslot = 0; uph ^= 1; }
+        if (v < 0) break;
       }
     }
     __syncwarp();
