@@ -631,16 +631,24 @@ struct QCfg : BCfg<D> {
   static constexpr int OFF_K = 2 * B::TILE;
   static constexpr int OFF_V = OFF_K + KSTAGE * B::TILE;
   static constexpr int OFF_BAR = OFF_V + VSTAGE * B::TILE;
-  static constexpr int N_BARS = 20;
+  static constexpr int N_BARS = 24;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
-  static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_UREC = OFF_MISC + 16;  // two unit records
+  static constexpr int SMEM_ALLOC = OFF_UREC + 2 * 64 + 1024;
   static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;
 };
 
 // KV_FULL[s] completes when K stage s and the V tile loaded with it have landed.
 enum { QB_Q_FULL = 0, QB_Q_EMPTY = 1, QB_KV_FULL = 2, QB_K_EMPTY = 5, QB_V_EMPTY = 8, QB_S_FULL = 10,
        QB_DP_FULL = 11, QB_S_READ = 12, QB_DS_FULL = 13, QB_ACC_FULL = 14, QB_ACC_EMPTY = 15,
-       QB_DRAIN = 16 };
+       QB_DRAIN = 16, QB_U_FULL = 17, QB_U_EMPTY = 19 };
+
+// dQ unit record (int32 words; slot stride 16 words): what every role needs to
+// run a unit, built once by the scheduler warp: the unit (< 0: no more work),
+// its query head and first row, its Q tile (bounds and documents), the cursor
+// standing on its first key tile, and the number of key tiles.
+enum { DR_V = 0, DR_H = 1, DR_Q0 = 2, DR_QT = 3, DR_CUR = 8, DR_NBLK = 14, DR_N = 15 };
+constexpr int DQ_UNIT_CONSUMERS = 10;  // producer, MMA lane, eight compute warps
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -659,12 +667,17 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* urec = reinterpret_cast<volatile int*>(smem + C::OFF_UREC);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(QB_Q_FULL), 1);
     mbar_init(bar(QB_Q_EMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(QB_U_FULL + s), 1);
+      mbar_init(bar(QB_U_EMPTY + s), DQ_UNIT_CONSUMERS);
+    }
     for (int s = 0; s < C::KSTAGE; ++s) {
       mbar_init(bar(QB_KV_FULL + s), 1);
       mbar_init(bar(QB_K_EMPTY + s), 1);
@@ -693,10 +706,31 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   const int G = f.Hq / f.Hkv;
   const unsigned long long tmo = f.timeout_ns;
 
-  // The unit's single Q tile; the second slot of the shared tile walk stays empty.
-  auto unit_tiles = [&](const UnitInfo& ui, QTile (&qt)[2]) {
-    qt[0] = make_qtile(f, ui, 0);
+  // Units reach every role as records in a two-slot ring (see DR_*). Reads
+  // one (the caller arrives on its slot's EMPTY barrier afterwards): false on
+  // a timeout. The unit's single Q tile is qt[0]; qt[1] stays empty.
+  auto read_unit = [&](int slot, uint32_t ph, int& v, int& h, int& q0, QTile (&qt)[2], Cursor& cur,
+                       int& nblk) -> bool {
+    if (!mbar_wait_bounded(bar(QB_U_FULL + slot), ph, tmo, f.err, abort_flag)) return false;
+    const volatile int* rs = urec + 16 * slot;
+    v = rs[DR_V];
+    if (v < 0) return true;
+    h = rs[DR_H];
+    q0 = rs[DR_Q0];
+    qt[0].qa = rs[DR_QT + 0];
+    qt[0].qb = rs[DR_QT + 1];
+    qt[0].ds = rs[DR_QT + 2];
+    qt[0].de = rs[DR_QT + 3];
+    qt[0].one_doc = rs[DR_QT + 4];
     qt[1].qa = qt[1].qb = qt[1].ds = qt[1].de = qt[1].one_doc = 0;
+    cur.item = rs[DR_CUR + 0];
+    cur.item_end = rs[DR_CUR + 1];
+    cur.kv_e = rs[DR_CUR + 2];
+    cur.k0 = rs[DR_CUR + 3];
+    cur.lo = rs[DR_CUR + 4];
+    cur.hi = rs[DR_CUR + 5];
+    nblk = rs[DR_NBLK];
+    return true;
   };
 
   if (warp == 0) {
@@ -706,18 +740,20 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       int armed_q = 0, armed_kv[C::KSTAGE] = {};
       uint32_t par_q = 0, par_kv[C::KSTAGE] = {};
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
-        const UnitInfo ui = unit_info(f, u);
+      for (;; ++unit_cnt) {
+        int v = -1, h = 0, q0 = 0, nblk = 0;
         QTile qt[2];
-        unit_tiles(ui, qt);
-        const int hk = ui.h / G;
+        Cursor cur;
+        if (!read_unit(unit_cnt & 1, (unit_cnt >> 1) & 1, v, h, q0, qt, cur, nblk)) { ok = false; break; }
+        mbar_arrive(bar(QB_U_EMPTY + (unit_cnt & 1)));
+        if (v < 0) break;
+        const int hk = h / G;
         if (!mbar_wait_bounded(bar(QB_Q_EMPTY), (unit_cnt & 1) ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(QB_Q_FULL), 2 * C::TILE);
         armed_q = 1;
         par_q = unit_cnt & 1;
-        load_rows128<D>(sQ, &tmq, bar(QB_Q_FULL), ui.h, ui.q0, f.T);
-        load_rows128<D>(sDO, &tmdo, bar(QB_Q_FULL), ui.h, ui.q0, f.T);
-        Cursor cur = make_cursor(f, ui, qt, f.causal);
+        load_rows128<D>(sQ, &tmq, bar(QB_Q_FULL), h, q0, f.T);
+        load_rows128<D>(sDO, &tmdo, bar(QB_Q_FULL), h, q0, f.T);
         int ka, kb, cls[2];
         while (next_tile(f, cur, qt, ka, kb, cls)) {
           const int st = kv_cnt % C::KSTAGE, vs = kv_cnt % C::VSTAGE;
@@ -731,6 +767,7 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
           load_rows128<D>(sv(kv_cnt), &tmv, bar(QB_KV_FULL + st), hk, ka, f.T);
           ++kv_cnt;
         }
+        if (!ok) break;
       }
       if (!ok) {
         volatile int no_abort = 0;
@@ -746,18 +783,15 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       const uint32_t tS = tmem + C::TM_S, tdP = tmem + C::TM_DP, tdQ = tmem + C::TM_DQ;
       uint32_t kv_cnt = 0, unit_cnt = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
-        const UnitInfo ui = unit_info(f, u);
+      for (;; ++unit_cnt) {
+        int v = -1, h = 0, q0 = 0, nblk = 0;
         QTile qt[2];
-        unit_tiles(ui, qt);
+        Cursor cur;
+        if (!read_unit(unit_cnt & 1, (unit_cnt >> 1) & 1, v, h, q0, qt, cur, nblk)) { ok = false; break; }
+        mbar_arrive(bar(QB_U_EMPTY + (unit_cnt & 1)));
+        if (v < 0) break;
         if (!mbar_wait_bounded(bar(QB_Q_FULL), unit_cnt & 1, tmo, f.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        int nblk = 0;
-        {
-          Cursor cur = make_cursor(f, ui, qt, f.causal);
-          int ka, kb, cls[2];
-          while (next_tile(f, cur, qt, ka, kb, cls)) ++nblk;
-        }
         if (nblk > 0) {
           const uint32_t g = kv_cnt;
           if (!mbar_wait_bounded(bar(QB_KV_FULL + g % C::KSTAGE), (g / C::KSTAGE) & 1, tmo, f.err,
@@ -804,6 +838,65 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       mbar_wait_bounded(bar(QB_DRAIN), 0, 50000000ull, f.err, &no_abort);
     }
     __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ unit scheduler
+    // Claims units (from the set-up kernel's queue, largest groups first, or
+    // strided over the CTAs) and builds each one's record ahead of the other
+    // roles: the table searches and the walk over the unit's items (to count
+    // its key tiles and find the first) are off their path.
+    if (lane == 0) {
+      int k_static = 0;
+      for (uint32_t cnt = 0;; ++cnt) {
+        int v;
+        if (f.work_counter) {
+          v = atomicAdd(f.work_counter, 1);
+        } else {
+          v = static_cast<int>(blockIdx.x) + k_static * static_cast<int>(gridDim.x);
+          ++k_static;
+        }
+        if (v >= n_units) v = -1;
+        int w[DR_N];
+        w[DR_V] = v;
+        if (v >= 0) {
+          const UnitInfo ui = unit_info(f, v);
+          QTile qt[2];
+          qt[0] = make_qtile(f, ui, 0);
+          qt[1].qa = qt[1].qb = qt[1].ds = qt[1].de = qt[1].one_doc = 0;
+          Cursor cur = make_cursor(f, ui, qt, f.causal);
+          Cursor walk = cur;
+          int ka, kb, cls[2], nblk = 0;
+          while (next_tile(f, walk, qt, ka, kb, cls)) {
+            if (nblk == 0) {
+              cur = walk;
+              cur.k0 = ka;  // standing on the first tile
+            }
+            ++nblk;
+          }
+          w[DR_H] = ui.h;
+          w[DR_Q0] = ui.q0;
+          w[DR_QT + 0] = qt[0].qa;
+          w[DR_QT + 1] = qt[0].qb;
+          w[DR_QT + 2] = qt[0].ds;
+          w[DR_QT + 3] = qt[0].de;
+          w[DR_QT + 4] = qt[0].one_doc;
+          w[DR_CUR + 0] = cur.item;
+          w[DR_CUR + 1] = cur.item_end;
+          w[DR_CUR + 2] = cur.kv_e;
+          w[DR_CUR + 3] = cur.k0;
+          w[DR_CUR + 4] = cur.lo;
+          w[DR_CUR + 5] = cur.hi;
+          w[DR_NBLK] = nblk;
+        }
+        const int slot = cnt & 1;
+        if (!mbar_wait_bounded(bar(QB_U_EMPTY + slot), ((cnt >> 1) & 1) ^ 1, tmo, f.err, abort_flag)) break;
+        volatile int* rs = urec + 16 * slot;
+        const int n = v >= 0 ? static_cast<int>(DR_N) : 1;
+        for (int i = 0; i < n; ++i) rs[i] = w[i];
+        mbar_arrive(bar(QB_U_FULL + slot));
+        if (v < 0) break;
+      }
+    }
+    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute
     const int wg = (warp - 4) >> 2;  // warpgroup: columns [64 wg, 64 wg + 64) of every block
@@ -816,24 +909,33 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     const float sl2 = f.scale_log2, scale = f.scale;
     uint32_t unit_cnt = 0, g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_cnt) {
-      const UnitInfo ui = unit_info(f, u);
+    for (;; ++unit_cnt) {
+      int v = -1, h = 0, q0 = 0, nblk_u = 0;
       QTile qt[2];
-      unit_tiles(ui, qt);
-      const int t = ui.q0 + r;
+      Cursor cur;
+      const bool got = read_unit(unit_cnt & 1, (unit_cnt >> 1) & 1, v, h, q0, qt, cur, nblk_u);
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+      if (lane == 0) mbar_arrive(bar(QB_U_EMPTY + (unit_cnt & 1)));
+      if (v < 0) break;
+      const int t = q0 + r;
       const bool valid = t >= qt[0].qa && t < qt[0].qb;
       int rds = 0, rde = 0;
       float nlse2 = 0.f, ndsc = 0.f;
       if (valid) {
-        const int dd = doc_of(f.cu, f.ndocs, t);
-        rds = __ldg(f.cu + dd);
-        rde = __ldg(f.cu + dd + 1);
-        nlse2 = __ldg(a.nlse2 + static_cast<size_t>(ui.h) * f.T + t);
-        ndsc = __ldg(a.ndsc + static_cast<size_t>(ui.h) * f.T + t);
+        if (qt[0].one_doc) {  // the tile's rows are all in one document
+          rds = qt[0].ds;
+          rde = qt[0].de;
+        } else {
+          const int dd = doc_of(f.cu, f.ndocs, t);
+          rds = __ldg(f.cu + dd);
+          rde = __ldg(f.cu + dd + 1);
+        }
+        nlse2 = __ldg(a.nlse2 + static_cast<size_t>(h) * f.T + t);
+        ndsc = __ldg(a.ndsc + static_cast<size_t>(h) * f.T + t);
       }
       const int rend = f.causal ? min(rde, t + 1) : rde;
       int nblk = 0;
-      Cursor cur = make_cursor(f, ui, qt, f.causal);
       int ka, kb, cls[2];
       while (next_tile(f, cur, qt, ka, kb, cls)) {
         const uint32_t ph = g & 1;
@@ -874,7 +976,7 @@ bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         uint32_t rq[32];
         if (nblk > 0) tmem_ld32_sync(tdQ + 32 * ch, rq);
         if (valid) {
-          uint16_t* dst = static_cast<uint16_t*>(a.dq) + (static_cast<size_t>(t) * f.Hq + ui.h) * D + 32 * ch;
+          uint16_t* dst = static_cast<uint16_t*>(a.dq) + (static_cast<size_t>(t) * f.Hq + h) * D + 32 * ch;
           if (nblk > 0) store_row32_bf16(dst, rq);
           else store_zero_row_bf16(dst, 32);
         }

@@ -312,6 +312,7 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   b.fwd.header = static_cast<const int32_t*>(workspace);
   b.fwd.segs = reinterpret_cast<const sp::SegEntry*>(static_cast<const char*>(workspace) + L.off_segs);
   b.fwd.rows_per_unit = sp::BWD_ROWS_PER_UNIT;
+  b.fwd.work_counter = static_cast<int32_t*>(workspace) + sp::WS_COUNTER;  // dQ units, reset by the set-up kernel
   b.lse = lse;
   b.ndsc = ndsc;
   b.nlse2 = nlse2;
