@@ -12,8 +12,10 @@
 // is split between the two CTAs' shared memory: the first holds keys 0-63 of
 // a K tile and dims 0-63 of a V tile, the second the other halves. Each SM
 // thus reads half a K/V tile per MMA from its own shared memory instead of a
-// whole one, and loads half of each tile, which is what limits the one-CTA
-// kernel (shared-memory bandwidth shared by the tensor core and TMA).
+// whole one and loads half of each tile (160 KB of shared-memory traffic per
+// key tile instead of 256 KB). Measured on the 32K-token layer, the MMAs take
+// as long as in the one-CTA kernel; what the pair gains is a shorter softmax
+// hand-off, and the freed shared memory holds a second Q buffer.
 //
 // Roles (12 warps per CTA):
 //   warp 0      TMA producer, in both CTAs: Q tiles of the CTA's head (two
