@@ -82,65 +82,10 @@ enum {
 };
 static_assert(B_U_EMPTY + 2 <= PCfg::N_BARS, "barrier slots");
 
-// A unit slot holds the unit's record: everything the roles need to walk it,
-// computed once by the first CTA's producer (one unit ahead of the others) and
-// stored into both CTAs' slot. Both CTAs' units have the same rows, documents
-// and items; the second CTA's query head is the first's plus one.
-constexpr int UREC_WORDS = 32;  // slot stride (int32 words)
-enum { UR_V = 0, UR_H = 1, UR_Q0 = 2, UR_QT = 3, UR_CUR = 13, UR_N = 19 };
-
-// The record's cursor stands on the unit's first tile (the producer has
-// walked to it), so a reader's first next_tile returns it without reading
-// any item.
-__device__ __forceinline__ void urec_pack(int v, const UnitInfo& ui, const QTile (&qt)[2], const Cursor& cur,
-                                          int (&w)[UR_N]) {
-  w[UR_V] = v;
-  w[UR_H] = ui.h;
-  w[UR_Q0] = ui.q0;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    w[UR_QT + 5 * i + 0] = qt[i].qa;
-    w[UR_QT + 5 * i + 1] = qt[i].qb;
-    w[UR_QT + 5 * i + 2] = qt[i].ds;
-    w[UR_QT + 5 * i + 3] = qt[i].de;
-    w[UR_QT + 5 * i + 4] = qt[i].one_doc;
-  }
-  w[UR_CUR + 0] = cur.item;
-  w[UR_CUR + 1] = cur.item_end;
-  w[UR_CUR + 2] = cur.kv_e;
-  w[UR_CUR + 3] = cur.k0;
-  w[UR_CUR + 4] = cur.lo;
-  w[UR_CUR + 5] = cur.hi;
-}
-
-// Reads a record (v >= 0) into the head of the reading CTA (rank), the unit's
-// first row, its Q tiles and the cursor.
-__device__ __forceinline__ void urec_read(const volatile int* rs, uint32_t rank, int& h, int& q0,
-                                          QTile (&qt)[2], Cursor& cur) {
-  h = rs[UR_H] + static_cast<int>(rank);
-  q0 = rs[UR_Q0];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    qt[i].qa = rs[UR_QT + 5 * i + 0];
-    qt[i].qb = rs[UR_QT + 5 * i + 1];
-    qt[i].ds = rs[UR_QT + 5 * i + 2];
-    qt[i].de = rs[UR_QT + 5 * i + 3];
-    qt[i].one_doc = rs[UR_QT + 5 * i + 4];
-  }
-  cur.item = rs[UR_CUR + 0];
-  cur.item_end = rs[UR_CUR + 1];
-  cur.kv_e = rs[UR_CUR + 2];
-  cur.k0 = rs[UR_CUR + 3];
-  cur.lo = rs[UR_CUR + 4];
-  cur.hi = rs[UR_CUR + 5];
-}
-
-// 32-byte global store.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-               :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                  "r"(w[7]) : "memory");
-}
+// A unit slot holds the unit's record (sp_tiles.cuh), built by the first CTA's
+// scheduler warp and stored into both CTAs' slot. Both CTAs' units have the
+// same rows, documents and items; the second CTA's query head is the first's
+// plus one.
 
 // Consumers of a unit slot: the producer, the MMA lane and 8 softmax warps of
 // the first CTA, the producer and 8 softmax warps of the second.
@@ -406,7 +351,7 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         const volatile int* rs = uring + UREC_WORDS * uslot;
         if (!wait_cl(bar(B_U_FULL + uslot), uph, tmo, a.err, abort_flag)) { ok = false; break; }
         const int v = rs[UR_V];
-        if (v >= 0) urec_read(rs, rank, h, q0, qt, cur);
+        if (v >= 0) read_unit_record(rs, static_cast<int>(rank), h, q0, qt, cur);
         arrive_cluster(lbar(B_U_EMPTY + uslot));
         if (++uslot == 2) { uslot = 0; uph ^= 1; }
         if (v < 0) break;
@@ -503,14 +448,7 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         const int v = fetch();
         int w[UR_N];
         w[UR_V] = v;
-        if (v >= 0) {
-          const UnitInfo ui = unit_info(a, 2 * v);
-          QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
-          Cursor cur = make_cursor(a, ui, qt, a.causal);
-          int ka = 0, kb = 0, cls[2];
-          if (next_tile(a, cur, qt, ka, kb, cls)) cur.k0 = ka;  // back onto the first tile
-          urec_pack(v, ui, qt, cur, w);
-        }
+        if (v >= 0) build_unit_record(a, 2 * v, v, w);
         if (!wait_cl(bar(B_U_EMPTY + uslot), uph ^ 1, tmo, a.err, abort_flag)) break;
         volatile int* rs = uring + UREC_WORDS * uslot;
         const int n = v >= 0 ? static_cast<int>(UR_N) : 1;
@@ -664,7 +602,7 @@ attn_tc_pair_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       int h = 0, q0 = 0;
       QTile qt[2];
       Cursor cur;
-      if (v >= 0) urec_read(rs, rank, h, q0, qt, cur);
+      if (v >= 0) read_unit_record(rs, static_cast<int>(rank), h, q0, qt, cur);
       __syncwarp();
       if (lane == 0) arrive_cluster(lbar(B_U_EMPTY + uslot));
       if (++uslot == 2) { uslot = 0; uph ^= 1; }

@@ -327,6 +327,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// 32-byte global store (p 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                  "r"(w[7]) : "memory");
+}
+
 // Three-input maximum.
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
   float d;

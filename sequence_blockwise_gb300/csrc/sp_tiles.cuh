@@ -109,4 +109,61 @@ __device__ __forceinline__ bool next_tile(const AttnArgs& a, Cursor& c, const QT
   }
 }
 
+// ---------------------------------------------------------------------------
+// Unit records: what every role of a forward kernel needs to run a unit,
+// built once by a scheduler warp and passed through shared memory, so that
+// the table searches (unit decode, the Q tiles' documents) and the walk over
+// the items to the unit's first tile stay off the other roles' path. Words:
+// the unit (< 0: no more work), its query head and first row, the two Q tiles
+// (bounds, documents), and the cursor standing on the first tile (a reader's
+// first next_tile returns that tile without reading an item).
+constexpr int UREC_WORDS = 32;  // slot stride (int32 words)
+enum { UR_V = 0, UR_H = 1, UR_Q0 = 2, UR_QT = 3, UR_CUR = 13, UR_N = 19 };
+
+__device__ __forceinline__ void build_unit_record(const AttnArgs& a, int unit, int v, int (&w)[UR_N]) {
+  const UnitInfo ui = unit_info(a, unit);
+  const QTile qt[2] = {make_qtile(a, ui, 0), make_qtile(a, ui, 1)};
+  Cursor cur = make_cursor(a, ui, qt, a.causal);
+  int ka = 0, kb = 0, cls[2];
+  if (next_tile(a, cur, qt, ka, kb, cls)) cur.k0 = ka;  // back onto the first tile
+  w[UR_V] = v;
+  w[UR_H] = ui.h;
+  w[UR_Q0] = ui.q0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    w[UR_QT + 5 * i + 0] = qt[i].qa;
+    w[UR_QT + 5 * i + 1] = qt[i].qb;
+    w[UR_QT + 5 * i + 2] = qt[i].ds;
+    w[UR_QT + 5 * i + 3] = qt[i].de;
+    w[UR_QT + 5 * i + 4] = qt[i].one_doc;
+  }
+  w[UR_CUR + 0] = cur.item;
+  w[UR_CUR + 1] = cur.item_end;
+  w[UR_CUR + 2] = cur.kv_e;
+  w[UR_CUR + 3] = cur.k0;
+  w[UR_CUR + 4] = cur.lo;
+  w[UR_CUR + 5] = cur.hi;
+}
+
+// Reads a record (unit >= 0); dh is added to the recorded query head.
+__device__ __forceinline__ void read_unit_record(const volatile int* rs, int dh, int& h, int& q0,
+                                                 QTile (&qt)[2], Cursor& cur) {
+  h = rs[UR_H] + dh;
+  q0 = rs[UR_Q0];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    qt[i].qa = rs[UR_QT + 5 * i + 0];
+    qt[i].qb = rs[UR_QT + 5 * i + 1];
+    qt[i].ds = rs[UR_QT + 5 * i + 2];
+    qt[i].de = rs[UR_QT + 5 * i + 3];
+    qt[i].one_doc = rs[UR_QT + 5 * i + 4];
+  }
+  cur.item = rs[UR_CUR + 0];
+  cur.item_end = rs[UR_CUR + 1];
+  cur.kv_e = rs[UR_CUR + 2];
+  cur.k0 = rs[UR_CUR + 3];
+  cur.lo = rs[UR_CUR + 4];
+  cur.hi = rs[UR_CUR + 5];
+}
+
 }  // namespace sp
