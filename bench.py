@@ -652,10 +652,14 @@ def main():
             result["cpu_baseline"] = None
         else:
             f, e, n, threads = oracle_sample(w, cu, args.cpu_seconds)
+            rate = f / e  # oracle FLOP/s over valid pairs
             result["cpu_baseline"] = {
-                "value": round(f / e / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+                "value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
                 "kind": "oracle",
                 "sample": f"{n} random query rows x {w.Hq} heads of {w.name}, fp64, {e:.1f} s",
+                # The whole workload at the sample's rate (rows are independent).
+                "full_workload_s": round(result["config"]["flop_per_step"] / rate, 1),
+                "gpu_ms_per_step": result["ms_per_step"],
             }
         print(json.dumps(result), flush=True)
     if world > 1:
