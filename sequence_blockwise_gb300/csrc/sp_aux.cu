@@ -207,9 +207,11 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
 }
 
 // Folds partial 2 into accumulator 1 in place, by the log-sum-exp rule. Each
-// warp handles UNROLL (row, head) pairs per pass and issues all their O loads
-// before any arithmetic, so that enough bytes are in flight to keep HBM busy
-// (the kernel is bandwidth bound: 12 bytes per O element).
+// warp handles UNROLL (row, head) pairs per pass and issues every load of the
+// pass (the LSE words and, for d <= 128, all of the O rows) before any of the
+// arithmetic that needs them, so that enough bytes are in flight to keep HBM
+// busy (the kernel is bandwidth bound: 12 bytes per O element). The merged LSE
+// words are stored at the end of the pass, after every lane has read them.
 constexpr int MERGE_UNROLL = 4;
 
 __global__ void __launch_bounds__(256)
@@ -223,39 +225,53 @@ lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
   const int nv = d >> 2;  // float4 per O row
   for (long long w0 = (static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * MERGE_UNROLL;
        w0 < n; w0 += wstride) {
-    // Weights of the UNROLL pairs.
-    float w1[MERGE_UNROLL], w2[MERGE_UNROLL];
+    size_t li[MERGE_UNROLL];
+    float l1[MERGE_UNROLL], l2[MERGE_UNROLL];
 #pragma unroll
     for (int k = 0; k < MERGE_UNROLL; ++k) {
       const long long w = w0 + k;
-      w1[k] = w2[k] = 0.f;
+      l1[k] = l2[k] = NEG_INF;
+      li[k] = 0;
       if (w >= n) continue;
       const int row = static_cast<int>(w / Hq), h = static_cast<int>(w % Hq);
-      const size_t li = static_cast<size_t>(h) * rows + row;
-      const float l1 = lse_acc[li], l2 = __ldg(lse_part + li);
-      const float M = fmaxf(l1, l2);
-      float L;
-      if (M == NEG_INF) {
-        L = NEG_INF;
-      } else {
-        const float e1 = expf(l1 - M), e2 = expf(l2 - M);
+      li[k] = static_cast<size_t>(h) * rows + row;
+      l1[k] = lse_acc[li[k]];
+      l2[k] = __ldg(lse_part + li[k]);
+    }
+    // The first float4 column of every O row (the only one when d <= 128).
+    float4 x[MERGE_UNROLL], y[MERGE_UNROLL];
+    if (lane < nv) {
+#pragma unroll
+      for (int k = 0; k < MERGE_UNROLL; ++k) {
+        if (w0 + k >= n) continue;
+        x[k] = reinterpret_cast<const float4*>(o_acc + static_cast<size_t>(w0 + k) * d)[lane];
+        y[k] = __ldg(reinterpret_cast<const float4*>(o_part + static_cast<size_t>(w0 + k) * d) + lane);
+      }
+    }
+    // Weights of the UNROLL pairs.
+    float w1[MERGE_UNROLL], w2[MERGE_UNROLL], L[MERGE_UNROLL];
+#pragma unroll
+    for (int k = 0; k < MERGE_UNROLL; ++k) {
+      const float M = fmaxf(l1[k], l2[k]);
+      w1[k] = w2[k] = 0.f;
+      L[k] = NEG_INF;
+      if (M != NEG_INF) {
+        const float e1 = expf(l1[k] - M), e2 = expf(l2[k] - M);
         const float s = e1 + e2;
-        L = M + logf(s);
+        L[k] = M + logf(s);
         const float inv = 1.f / s;
         w1[k] = e1 * inv;
         w2[k] = e2 * inv;
       }
-      __syncwarp();
-      if (lane == 0) lse_acc[li] = L;
     }
-    // O rows: all loads first, then the combined writes.
     for (int c = lane; c < nv; c += 32) {
-      float4 x[MERGE_UNROLL], y[MERGE_UNROLL];
+      if (c != lane) {
 #pragma unroll
-      for (int k = 0; k < MERGE_UNROLL; ++k) {
-        if (w0 + k >= n) continue;
-        x[k] = reinterpret_cast<const float4*>(o_acc + static_cast<size_t>(w0 + k) * d)[c];
-        y[k] = __ldg(reinterpret_cast<const float4*>(o_part + static_cast<size_t>(w0 + k) * d) + c);
+        for (int k = 0; k < MERGE_UNROLL; ++k) {
+          if (w0 + k >= n) continue;
+          x[k] = reinterpret_cast<const float4*>(o_acc + static_cast<size_t>(w0 + k) * d)[c];
+          y[k] = __ldg(reinterpret_cast<const float4*>(o_part + static_cast<size_t>(w0 + k) * d) + c);
+        }
       }
 #pragma unroll
       for (int k = 0; k < MERGE_UNROLL; ++k) {
@@ -264,6 +280,13 @@ lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
             make_float4(w1[k] * x[k].x + w2[k] * y[k].x, w1[k] * x[k].y + w2[k] * y[k].y,
                         w1[k] * x[k].z + w2[k] * y[k].z, w1[k] * x[k].w + w2[k] * y[k].w);
       }
+    }
+    // Every lane has read the accumulator's LSE words of this pass.
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < MERGE_UNROLL; ++k)
+        if (w0 + k < n) lse_acc[li[k]] = L[k];
     }
   }
 }
