@@ -35,68 +35,73 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def _bind(lib):
+    """Declares the argument and result types of every exported function of a
+    loaded oracle library (the built one, or a test's variant of the source)."""
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    vp = ctypes.c_void_p
+    lib.oracle_attn.restype = ctypes.c_int
+    lib.oracle_attn.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_double, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                ctypes.c_int, f64p, f64p, ctypes.c_int]
+    lib.oracle_attn_backward.restype = ctypes.c_int
+    lib.oracle_attn_backward.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_double, f64p, f64p, f64p,
+                                         ctypes.c_int]
+    lib.oracle_attn_backward_sampled.restype = ctypes.c_int
+    lib.oracle_attn_backward_sampled.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_double, i32p,
+                                                 ctypes.c_int, f64p, i32p, ctypes.c_int, f64p, f64p,
+                                                 ctypes.c_int]
+    lib.oracle_lse_merge.restype = None
+    lib.oracle_lse_merge.argtypes = [f64p, f64p, f64p, f64p, ctypes.c_longlong, ctypes.c_int,
+                                     f64p, f64p]
+    lib.oracle_valid_pairs.restype = ctypes.c_longlong
+    lib.oracle_valid_pairs.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.oracle_closed_form_schedule.restype = ctypes.c_longlong
+    lib.oracle_closed_form_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                                ctypes.c_int, ctypes.c_int, i32p,
+                                                ctypes.c_longlong]
+    lib.oracle_check_hamiltonian.restype = ctypes.c_int
+    lib.oracle_check_hamiltonian.argtypes = [ctypes.c_int, i32p]
+    lib.oracle_check_schedule.restype = ctypes.c_int
+    lib.oracle_check_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                          ctypes.c_int, ctypes.c_int, i32p, ctypes.c_longlong,
+                                          i32p, ctypes.c_int, ctypes.c_char_p, ctypes.c_int, i32p]
+    lib.oracle_check_hier_schedule.restype = ctypes.c_int
+    lib.oracle_check_hier_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, i32p,
+                                               i32p, ctypes.c_longlong, i32p, ctypes.c_int,
+                                               ctypes.c_char_p, ctypes.c_int, i32p]
+    lib.oracle_link_bytes_hier.restype = ctypes.c_int
+    lib.oracle_link_bytes_hier.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                           ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)]
+    lib.oracle_chunk_bounds.restype = ctypes.c_int
+    lib.oracle_chunk_bounds.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                        ctypes.c_int, i32p]
+    lib.oracle_link_bytes.restype = ctypes.c_int
+    lib.oracle_link_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                      ctypes.c_int, i32p, ctypes.c_longlong, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_longlong)]
+    lib.oracle_check_cu_seqlens.restype = ctypes.c_int
+    lib.oracle_check_cu_seqlens.argtypes = [i32p, ctypes.c_int, ctypes.c_int]
+    lib.oracle_doc_of.restype = ctypes.c_int
+    lib.oracle_doc_of.argtypes = [i32p, ctypes.c_int, ctypes.c_int]
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB)
-        i32p = ctypes.POINTER(ctypes.c_int32)
-        f64p = ctypes.POINTER(ctypes.c_double)
-        vp = ctypes.c_void_p
-        lib.oracle_attn.restype = ctypes.c_int
-        lib.oracle_attn.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                    ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
-                                    ctypes.c_double, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
-                                    ctypes.c_int, f64p, f64p, ctypes.c_int]
-        lib.oracle_attn_backward.restype = ctypes.c_int
-        lib.oracle_attn_backward.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                             ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
-                                             ctypes.c_int, ctypes.c_double, f64p, f64p, f64p,
-                                             ctypes.c_int]
-        lib.oracle_attn_backward_sampled.restype = ctypes.c_int
-        lib.oracle_attn_backward_sampled.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
-                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
-                                                     ctypes.c_int, ctypes.c_int, ctypes.c_double, i32p,
-                                                     ctypes.c_int, f64p, i32p, ctypes.c_int, f64p, f64p,
-                                                     ctypes.c_int]
-        lib.oracle_lse_merge.restype = None
-        lib.oracle_lse_merge.argtypes = [f64p, f64p, f64p, f64p, ctypes.c_longlong, ctypes.c_int,
-                                         f64p, f64p]
-        lib.oracle_valid_pairs.restype = ctypes.c_longlong
-        lib.oracle_valid_pairs.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                           ctypes.c_int, ctypes.c_int, ctypes.c_int]
-        lib.oracle_closed_form_schedule.restype = ctypes.c_longlong
-        lib.oracle_closed_form_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
-                                                    ctypes.c_int, ctypes.c_int, i32p,
-                                                    ctypes.c_longlong]
-        lib.oracle_check_hamiltonian.restype = ctypes.c_int
-        lib.oracle_check_hamiltonian.argtypes = [ctypes.c_int, i32p]
-        lib.oracle_check_schedule.restype = ctypes.c_int
-        lib.oracle_check_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
-                                              ctypes.c_int, ctypes.c_int, i32p, ctypes.c_longlong,
-                                              i32p, ctypes.c_int, ctypes.c_char_p, ctypes.c_int, i32p]
-        lib.oracle_check_hier_schedule.restype = ctypes.c_int
-        lib.oracle_check_hier_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                   ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, i32p,
-                                                   i32p, ctypes.c_longlong, i32p, ctypes.c_int,
-                                                   ctypes.c_char_p, ctypes.c_int, i32p]
-        lib.oracle_link_bytes_hier.restype = ctypes.c_int
-        lib.oracle_link_bytes_hier.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
-                                               ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
-                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                               ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)]
-        lib.oracle_chunk_bounds.restype = ctypes.c_int
-        lib.oracle_chunk_bounds.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
-                                            ctypes.c_int, i32p]
-        lib.oracle_link_bytes.restype = ctypes.c_int
-        lib.oracle_link_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
-                                          ctypes.c_int, i32p, ctypes.c_longlong, ctypes.c_int,
-                                          ctypes.POINTER(ctypes.c_longlong)]
-        lib.oracle_check_cu_seqlens.restype = ctypes.c_int
-        lib.oracle_check_cu_seqlens.argtypes = [i32p, ctypes.c_int, ctypes.c_int]
-        lib.oracle_doc_of.restype = ctypes.c_int
-        lib.oracle_doc_of.argtypes = [i32p, ctypes.c_int, ctypes.c_int]
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(_LIB))
     return _lib
 
 

@@ -1,0 +1,131 @@
+"""Planted mistakes in the oracle are caught by its pins.
+
+Each mutant is a copy of oracle/oracle.cpp with one plausible mistake planted
+in it: a mask off by one, the document start ignored, a wrong GQA head map, a
+dropped scale or maximum, a transposed operand, a wrong merge weight, a wrong
+sign, term or operand in a gradient. Each copy is compiled on the CPU into a
+temporary library. Every parameterisation of the pin tests in
+test_oracle_pins.py and test_oracle_backward_pins.py then runs with the
+oracle module pointed at that library, and at least one of them must fail.
+The unmodified oracle passes the same list (the control), so a failure means
+the pins caught the mistake, not that the harness broke."""
+import contextlib
+import ctypes
+import itertools
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_backward_pins
+import test_oracle_pins
+
+# name -> (text in oracle.cpp, replacement); each text occurs exactly once.
+MUTANTS = {
+    "causal_mask_excludes_diagonal": ("      if (causal) j1 = std::min(j1, i + 1);\n      double* o_row",
+                                      "      if (causal) j1 = std::min(j1, i);\n      double* o_row"),
+    "document_start_ignored": ("      int j0 = std::max(cu[D], kv_begin);",
+                               "      int j0 = std::max(0, kv_begin);"),
+    "gqa_head_map_interleaved": ("      const int g = h / G;\n      // V(i)",
+                                 "      const int g = h % Hkv;\n      // V(i)"),
+    "scale_dropped": ("        s[j - j0] = dot * scale;\n        m = std::max(m, s[j - j0]);\n      }\n      double sum",
+                      "        s[j - j0] = dot;\n        m = std::max(m, s[j - j0]);\n      }\n      double sum"),
+    "lse_without_maximum": ("      const double lse = m + std::log(sum);\n      std::fill(acc",
+                            "      const double lse = std::log(sum);\n      std::fill(acc"),
+    "values_read_from_keys": ("        for (int c = 0; c < d; ++c) acc[c] += w * widen(v, dtype, vb + c);",
+                              "        for (int c = 0; c < d; ++c) acc[c] += w * widen(k, dtype, vb + c);"),
+    "merge_weight_offset": ("    const double wa = std::exp(a - L), wb = std::exp(b - L);",
+                            "    const double wa = std::exp(a - M), wb = std::exp(b - L);"),
+    "ds_sign_flipped": ("          const double ds = pij * (dp - Di);",
+                        "          const double ds = pij * (Di - dp);"),
+    "ds_without_rowdot": ("          const double ds = pij * (dp - Di);",
+                          "          const double ds = pij * dp;"),
+    "dk_from_output_gradient": ("            dk_out[kb + c] += scale * ds * qi[c];",
+                                "            dk_out[kb + c] += scale * ds * doi[c];"),
+    "dq_without_scale": ("            dq_out[qb + c] += scale * ds * widen(k, dtype, kb + c);",
+                         "            dq_out[qb + c] += ds * widen(k, dtype, kb + c);"),
+    "dv_from_ds": ("            dv_out[kb + c] += pij * doi[c];",
+                   "            dv_out[kb + c] += ds * doi[c];"),
+    "dp_from_keys": ("          for (int c = 0; c < d; ++c) dp += doi[c] * widen(v, dtype, kb + c);",
+                     "          for (int c = 0; c < d; ++c) dp += doi[c] * widen(k, dtype, kb + c);"),
+    "sampled_dp_is_the_score": ("  *dp = dpd;", "  *dp = dot;"),
+    "valid_pairs_causal_off_by_one": ("      const int hi = std::min(c1, i + 1);\n      if (hi > c0)",
+                                      "      const int hi = std::min(c1, i);\n      if (hi > c0)"),
+}
+
+
+def _pin_calls():
+    """(label, function, kwargs) for every parameterisation of every pin test."""
+    calls = []
+    for mod in (test_oracle_pins, test_oracle_backward_pins):
+        for name in sorted(dir(mod)):
+            fn = getattr(mod, name)
+            if not name.startswith("test_") or not callable(fn):
+                continue
+            grids = []
+            for mark in getattr(fn, "pytestmark", []):
+                if mark.name != "parametrize":
+                    continue
+                names = [n.strip() for n in mark.args[0].split(",")]
+                values = list(mark.args[1])
+                grids.append([dict(zip(names, v if len(names) > 1 else (v,))) for v in values])
+            for combo in itertools.product(*grids) if grids else [()]:
+                kw = {}
+                for part in combo:
+                    kw.update(part)
+                calls.append((f"{mod.__name__}.{name}{kw or ''}", fn, kw))
+    return calls
+
+
+def _failing_pins():
+    failed = []
+    for label, fn, kw in _pin_calls():
+        try:
+            with np.errstate(all="ignore"):  # wrong arithmetic may yield inf - inf
+                fn(**kw)
+        except Exception:  # an assertion, or an error the wrong arithmetic provoked
+            failed.append(label)
+    return failed
+
+
+@contextlib.contextmanager
+def _oracle_library(path):
+    saved = oracle._lib
+    oracle._lib = oracle._bind(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        oracle._lib = saved
+
+
+@pytest.fixture(scope="module")
+def mutant_libs(tmp_path_factory):
+    src = open(oracle._SRC).read()
+    d = tmp_path_factory.mktemp("oracle_mutants")
+    procs, libs = [], {}
+    for name, (old, new) in MUTANTS.items():
+        assert src.count(old) == 1, f"mutation {name}: target text not found exactly once"
+        cpp = os.path.join(d, f"{name}.cpp")
+        with open(cpp, "w") as f:
+            f.write(src.replace(old, new))
+        libs[name] = os.path.join(d, f"lib{name}.so")
+        procs.append(subprocess.Popen(["g++", "-O1", "-std=c++17", "-fopenmp", "-fPIC", "-shared", cpp,
+                                       "-o", libs[name]]))
+    for p in procs:
+        assert p.wait() == 0
+    return libs
+
+
+def test_unmodified_oracle_passes_every_pin():
+    assert len(_pin_calls()) >= 25
+    assert _failing_pins() == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(mutant_libs, name):
+    with _oracle_library(mutant_libs[name]):
+        failed = _failing_pins()
+    print(f"{name}: caught by {len(failed)} pin(s): {failed[:4]}")
+    assert failed, f"no pin caught the planted mistake {name}"
