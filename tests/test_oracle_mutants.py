@@ -3,10 +3,14 @@
 Each mutant is a copy of oracle/oracle.cpp with one plausible mistake planted
 in it: a mask off by one, the document start ignored, a wrong GQA head map, a
 dropped scale or maximum, a transposed operand, a wrong merge weight, a wrong
-sign, term or operand in a gradient. Each copy is compiled on the CPU into a
-temporary library. Every parameterisation of the pin tests in
-test_oracle_pins.py and test_oracle_backward_pins.py then runs with the
-oracle module pointed at that library, and at least one of them must fail.
+sign, term or operand in a gradient; in the schedule closed forms and checks,
+a reversed ring order, another zigzag layout, the remainder tokens given to
+the last pieces, a check dropped or weakened, the TASP source walked the wrong
+way round the cycle. Each copy is compiled on the CPU into a temporary
+library. Every parameterisation of the pin tests in test_oracle_pins.py,
+test_oracle_backward_pins.py and test_oracle_schedule_pins.py (which call the
+oracle only, never the product) then runs with the oracle module pointed at
+that library, and at least one of them must fail.
 The unmodified oracle passes the same list (the control), so a failure means
 the pins caught the mistake, not that the harness broke."""
 import contextlib
@@ -21,6 +25,7 @@ import pytest
 import oracle
 import test_oracle_backward_pins
 import test_oracle_pins
+import test_oracle_schedule_pins
 
 # name -> (text in oracle.cpp, replacement); each text occurs exactly once.
 MUTANTS = {
@@ -53,13 +58,29 @@ MUTANTS = {
     "sampled_dp_is_the_score": ("  *dp = dpd;", "  *dp = dot;"),
     "valid_pairs_causal_off_by_one": ("      const int hi = std::min(c1, i + 1);\n      if (hi > c0)",
                                       "      const int hi = std::min(c1, i);\n      if (hi > c0)"),
+    # Schedules: the closed forms and the checks.
+    "ring_order_reversed": ("        const int src = ((r - s) % P + P) % P;\n        int ka, kb;",
+                            "        const int src = ((r + s) % P + P) % P;\n        int ka, kb;"),
+    "zigzag_mirror_chunk": ("      const int mine[2] = {r, 2 * P - 1 - r};",
+                            "      const int mine[2] = {r, P + r};"),
+    "piece_remainder_to_last": ("  *b = idx * base + std::min(idx, extra);\n  *e = *b + base + (idx < extra ? 1 : 0);",
+                                "  *b = idx * base + std::max(0, idx - (parts - extra));\n"
+                                "  *e = *b + base + (idx >= parts - extra ? 1 : 0);"),
+    "hamiltonian_arc_reuse_unchecked": ("      if (++cnt > 1) return 3;", "      ++cnt;"),
+    "hamiltonian_revisit_unchecked": ("      if (seen[u]) return 2;\n", ""),
+    "overlap_check_weakened": ("        if (ks[y].first < ks[y - 1].second) return fail(8,",
+                               "        if (ks[y].first < ks[y - 1].first) return fail(8,"),
+    "pruning_check_dropped": ("    if (oracle_valid_pairs(cu, ndocs, causal, qa, qb, ka, kb) == 0)\n      return fail(4,",
+                              "    if (false)\n      return fail(4,"),
+    "tasp_source_walks_forward": ("        for (int t = 0; t < s; ++t) src = pred[static_cast<size_t>(c) * P + src];",
+                                  "        for (int t = 0; t < s; ++t) src = succ[static_cast<size_t>(c) * P + src];"),
 }
 
 
 def _pin_calls():
     """(label, function, kwargs) for every parameterisation of every pin test."""
     calls = []
-    for mod in (test_oracle_pins, test_oracle_backward_pins):
+    for mod in (test_oracle_pins, test_oracle_backward_pins, test_oracle_schedule_pins):
         for name in sorted(dir(mod)):
             fn = getattr(mod, name)
             if not name.startswith("test_") or not callable(fn):

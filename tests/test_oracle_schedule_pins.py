@@ -81,6 +81,14 @@ def test_hamiltonian_check_rejects_defects():
     bad = good.copy()
     bad[2, 3] = 3                         # self loop
     assert oracle.check_hamiltonian(5, bad) == 1
+    # Rows whose walk from vertex 0 is back at 0 after P arcs without having
+    # visited every vertex (the cycle through 0 is shorter and its length
+    # divides P). K_4* split into three factors of two 2-cycles uses every arc
+    # exactly once and is still not a decomposition into Hamiltonian cycles.
+    two_cycle_factors = np.array([[1, 0, 3, 2], [2, 3, 0, 1], [3, 2, 1, 0]], dtype=np.int32)
+    assert oracle.check_hamiltonian(4, two_cycle_factors) == 2
+    two_triangles = np.array([[1, 2, 0, 4, 5, 3]] + [[(u + 1) % 6 for u in range(6)]] * 4, dtype=np.int32)
+    assert oracle.check_hamiltonian(6, two_triangles) == 2
 
 
 def _split(n, parts, idx):
