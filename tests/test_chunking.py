@@ -30,7 +30,7 @@ def _work_prefix(cu, causal, t):
 
 
 @pytest.mark.parametrize("T,P", [(32768, 8), (1000, 7), (5, 8), (129, 2), (65536, 16)])
-def test_single_doc_causal_closed_form(T, P):
+def test_oracle_single_doc_causal_closed_form(T, P):
     cu = np.array([0, T])
     got = [int(x) for x in oracle.chunk_bounds(1, P, T, cu, True)]
     total = T * (T + 1) // 2
@@ -46,7 +46,7 @@ def test_single_doc_causal_closed_form(T, P):
 
 
 @pytest.mark.parametrize("T,P", [(65536, 16), (1000, 7), (3, 5)])
-def test_single_doc_full_mask_closed_form(T, P):
+def test_oracle_single_doc_full_mask_closed_form(T, P):
     got = [int(x) for x in oracle.chunk_bounds(1, P, T, np.array([0, T]), False)]
     assert got == [0] + [-(-r * T // P) for r in range(1, P)] + [T]
 
@@ -57,7 +57,7 @@ def _random_cu(rng, T, ndocs):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_packed_balance_invariant(causal):
+def test_oracle_packed_balance_invariant(causal):
     rng = np.random.default_rng(3)
     for _ in range(40):
         T = int(rng.integers(2, 3000))
@@ -72,7 +72,7 @@ def test_packed_balance_invariant(causal):
         assert np.all(np.diff(b) >= 0)
 
 
-def test_doc_snap_rule():
+def test_oracle_doc_snap_rule():
     """Mode 2 restated with the per-document closed form of W: bound r moves to
     the document start nearest in work when that moves at most W(T) / (16P)."""
     rng = np.random.default_rng(8)

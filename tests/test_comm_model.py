@@ -12,23 +12,26 @@ import sequence_blockwise_gb300 as sb
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def test_hand_derived_ring_needed_only():
-    got = sb.sp_schedule_link_bytes(sb.SP_SCHED_RING, 4, 256, [0, 256], True, needed_only=True)
+def _hand_derived_ring_needed_only():
     exp = np.zeros((3, 4, 4), dtype=np.int64)
     for line in open(os.path.join(GOLDEN, "ring_P4_T256_causal_needed_link_bytes.txt")):
         if line.strip() and not line.startswith("#"):
             t, u, v, b = (int(x) for x in line.split())
             exp[t - 1, u, v] = b
-    assert np.array_equal(got, exp)
-    assert np.array_equal(oracle.link_bytes(0, 4, 256, [0, 256], True, needed_only=True), exp)
+    return exp
 
 
-@pytest.mark.parametrize("P", [2, 3, 5, 7, 8, 16])
-def test_closed_forms_full_allgather(P):
-    T = P * (P - 1) * 12 + 5 * P  # chunks and pieces not all equal
-    cu = [0, T]
-    ring = sb.sp_schedule_link_bytes(sb.SP_SCHED_RING, P, T, cu, False, bytes_per_token=4)
-    tasp = sb.sp_schedule_link_bytes(sb.SP_SCHED_TASP, P, T, cu, False, bytes_per_token=4)
+def test_hand_derived_ring_needed_only():
+    got = sb.sp_schedule_link_bytes(sb.SP_SCHED_RING, 4, 256, [0, 256], True, needed_only=True)
+    assert np.array_equal(got, _hand_derived_ring_needed_only())
+
+
+def test_oracle_hand_derived_ring_needed_only():
+    got = oracle.link_bytes(0, 4, 256, [0, 256], True, needed_only=True)
+    assert np.array_equal(got, _hand_derived_ring_needed_only())
+
+
+def _full_allgather_closed_forms(ring, tasp, P, T):
     # Every token is delivered to the P-1 other ranks: same total for both.
     assert ring.sum() == tasp.sum() == 4 * T * (P - 1)
     # Ring: each iteration uses exactly the P ring links; TASP: all P(P-1) links.
@@ -41,6 +44,27 @@ def test_closed_forms_full_allgather(P):
     chunk = -(-T // P)
     piece = -(-chunk // (P - 1))
     assert ring.max() == 4 * chunk and tasp.max() == 4 * piece
+
+
+@pytest.mark.parametrize("P", [2, 3, 5, 7, 8, 16])
+def test_closed_forms_full_allgather(P):
+    T = P * (P - 1) * 12 + 5 * P  # chunks and pieces not all equal
+    cu = [0, T]
+    ring = sb.sp_schedule_link_bytes(sb.SP_SCHED_RING, P, T, cu, False, bytes_per_token=4)
+    tasp = sb.sp_schedule_link_bytes(sb.SP_SCHED_TASP, P, T, cu, False, bytes_per_token=4)
+    _full_allgather_closed_forms(ring, tasp, P, T)
+
+
+@pytest.mark.parametrize("P", [2, 3, 5, 7])
+def test_oracle_closed_forms_full_allgather(P):
+    """The same closed forms for the oracle's model, with the decomposition
+    u -> u + s (s = 1 .. P-1) into Hamiltonian cycles for prime P."""
+    T = P * (P - 1) * 12 + 5 * P
+    cu = [0, T]
+    succ = np.array([[(u + s) % P for u in range(P)] for s in range(1, P)], dtype=np.int32)
+    ring = oracle.link_bytes(0, P, T, cu, False, bytes_per_token=4)
+    tasp = oracle.link_bytes(2, P, T, cu, False, succ=succ, bytes_per_token=4)
+    _full_allgather_closed_forms(ring, tasp, P, T)
 
 
 def _rand_cu(rng, T, nd):

@@ -7,10 +7,15 @@ sign, term or operand in a gradient; in the schedule closed forms and checks,
 a reversed ring order, another zigzag layout, the remainder tokens given to
 the last pieces, a check dropped or weakened, the TASP source walked the wrong
 way round the cycle. Each copy is compiled on the CPU into a temporary
-library. Every parameterisation of the pin tests in test_oracle_pins.py,
-test_oracle_backward_pins.py and test_oracle_schedule_pins.py (which call the
-oracle only, never the product) then runs with the oracle module pointed at
-that library, and at least one of them must fail.
+library. Every parameterisation of the oracle's pin tests then runs with the
+oracle module pointed at that library, and at least one of them must fail:
+all of test_oracle_pins.py, test_oracle_backward_pins.py and
+test_oracle_schedule_pins.py, and the test_oracle_* functions of
+test_chunking.py and test_comm_model.py (these call the oracle only, never
+the product). Mistakes are also planted in the chunk bounds (a balance bound
+off by one, a causal row's work off by one, the document-snap threshold) and
+in the communication model (the ring's sender, the source walked forward, the
+needed-only look-ahead cut short, a TASP piece counted as a whole chunk).
 The unmodified oracle passes the same list (the control), so a failure means
 the pins caught the mistake, not that the harness broke."""
 import contextlib
@@ -23,9 +28,17 @@ import numpy as np
 import pytest
 
 import oracle
+import test_chunking
+import test_comm_model
 import test_oracle_backward_pins
 import test_oracle_pins
 import test_oracle_schedule_pins
+
+# Modules of oracle pins, and the prefix of their test functions that run the
+# oracle alone (the chunking and communication modules also test the product).
+PIN_MODULES = [(test_oracle_pins, "test_"), (test_oracle_backward_pins, "test_"),
+               (test_oracle_schedule_pins, "test_"), (test_chunking, "test_oracle_"),
+               (test_comm_model, "test_oracle_")]
 
 # name -> (text in oracle.cpp, replacement); each text occurs exactly once.
 MUTANTS = {
@@ -74,16 +87,31 @@ MUTANTS = {
                               "    if (false)\n      return fail(4,"),
     "tasp_source_walks_forward": ("        for (int t = 0; t < s; ++t) src = pred[static_cast<size_t>(c) * P + src];",
                                   "        for (int t = 0; t < s; ++t) src = succ[static_cast<size_t>(c) * P + src];"),
+    # Chunk bounds (load-balanced chunking).
+    "chunk_balance_off_by_one": (
+        "    while (t < T && static_cast<long long>(P) * W[t] < static_cast<long long>(r) * W[T]) ++t;",
+        "    while (t < T && static_cast<long long>(P) * W[t] <= static_cast<long long>(r) * W[T]) ++t;"),
+    "chunk_causal_work_off_by_one": ("    const long long n = causal ? (i - cu[D] + 1) : (cu[D + 1] - cu[D]);",
+                                     "    const long long n = causal ? (i - cu[D]) : (cu[D + 1] - cu[D]);"),
+    "chunk_snap_threshold_halved": ("      if (16LL * P * bdist <= W[T] && best > out[r - 1]) out[r] = best;",
+                                    "      if (8LL * P * bdist <= W[T] && best > out[r - 1]) out[r] = best;"),
+    # Communication model (bytes per link per iteration).
+    "link_ring_sender_reversed": ("        const int from = (r + P - 1) % P;", "        const int from = (r + 1) % P;"),
+    "link_source_walks_forward": ("        const int src_rank = ((r - t) % P + P) % P;  // whose chunk(s) arrive",
+                                  "        const int src_rank = ((r + t) % P + P) % P;  // whose chunk(s) arrive"),
+    "link_lookahead_short": ("          for (int k = 0; !keep && t + k <= P - 1; ++k)\n            if (wants((r + k) % P",
+                             "          for (int k = 0; !keep && t + k < P - 1; ++k)\n            if (wants((r + k) % P"),
+    "link_tasp_piece_as_chunk": ("                (kb - ka) * bytes_per_token;", "                (ce - cb) * bytes_per_token;"),
 }
 
 
 def _pin_calls():
     """(label, function, kwargs) for every parameterisation of every pin test."""
     calls = []
-    for mod in (test_oracle_pins, test_oracle_backward_pins, test_oracle_schedule_pins):
+    for mod, prefix in PIN_MODULES:
         for name in sorted(dir(mod)):
             fn = getattr(mod, name)
-            if not name.startswith("test_") or not callable(fn):
+            if not name.startswith(prefix) or not callable(fn):
                 continue
             grids = []
             for mark in getattr(fn, "pytestmark", []):
