@@ -129,3 +129,82 @@ def test_hier_link_bytes_closed_forms():
     assert not intra.any()
     flat = sb.sp_schedule_link_bytes(sb.SP_SCHED_RING, R, T, cu, True, bytes_per_token=2 * Hkv * d * 2)
     assert np.array_equal(inter, flat)
+
+
+# ------------------------------------------------------------------ oracle-only pins
+# These call the oracle alone: the two-level items are restated here from the
+# oracle's flat closed form (pinned by hand-derived lists), and the
+# communication counts are written down by hand.
+
+def _restated_hier(kind, R, U, Hq, T, cu, causal):
+    """Every item of group g of the flat R-rank schedule, held by the U ranks
+    g*U + u, each for query heads [u Hq/U, (u+1) Hq/U)."""
+    flat = oracle.closed_form_schedule(kind, R, T, cu, causal)
+    hs = Hq // U
+    items, heads = [], []
+    for it in flat:
+        for u in range(U):
+            x = it.copy()
+            x[0] = it[0] * U + u
+            items.append(x)
+            heads.append([u * hs, (u + 1) * hs])
+    return np.array(items, dtype=np.int32).reshape(-1, 8), np.array(heads, dtype=np.int32).reshape(-1, 2)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("kind,R,U,Hq", [(0, 2, 4, 8), (1, 2, 2, 4), (0, 3, 2, 6), (0, 1, 4, 8), (1, 3, 1, 2)])
+def test_oracle_hier_check_accepts_restated_schedules(kind, R, U, Hq, causal):
+    T = 240
+    cu = np.array([0, 50, 51, 180, 240], dtype=np.int32)
+    items, heads = _restated_hier(kind, R, U, Hq, T, cu, causal)
+    rc, msg = oracle.check_hier_schedule(kind, R, U, Hq, T, cu, causal, items, heads, brute=True)
+    assert rc == 0, msg
+
+
+def test_oracle_hier_check_rejects_defects_on_restated_schedule():
+    T, Hq, R, U = 240, 8, 2, 4
+    hs = Hq // U
+    cu = np.array([0, 100, 240], dtype=np.int32)
+    items, heads = _restated_hier(0, R, U, Hq, T, cu, True)
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, items, heads, brute=True)[0] == 0
+    x = int(np.nonzero(items[:, 0] % U == 1)[0][0])
+    bad = heads.copy()
+    bad[x] = heads[x] + hs                       # another slice's heads
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, items, bad)[0] == 22
+    bad = heads.copy()
+    bad[x, 1] -= 1                               # right start, one head short
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, items, bad)[0] == 22
+    keep = np.ones(len(items), dtype=bool)       # slice 1 loses an item
+    keep[np.nonzero(items[:, 0] % U == 1)[0][-1]] = False
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, items[keep], heads[keep])[0] == 39
+    dup_i = np.concatenate([items, items[x:x + 1]])
+    dup_h = np.concatenate([heads, heads[x:x + 1]])
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, dup_i, dup_h)[0] == 38
+    big = items.copy()
+    big[0, 0] = R * U
+    assert oracle.check_hier_schedule(0, R, U, Hq, T, cu, True, big, heads)[0] == 21
+
+
+def test_oracle_hier_link_bytes_closed_forms():
+    """One group over U = 4 ranks of unequal token counts (510 = 128 + 128 +
+    127 + 127): rank a sends rank b the q and the k, v of a's tokens for b's
+    heads, and returns to b the o of b's tokens for a's heads, so
+    intra[a, b] = n_a (hs + 2 kvs) d eb + n_b hs d eb. One rank per group: no
+    all-to-all, and the Inter-SP traffic is the flat model's with k and v of
+    every key/value head per token."""
+    T, U, Hq, Hkv, d, eb = 510, 4, 8, 2, 64, 2
+    cu = np.array([0, T], dtype=np.int32)
+    intra, inter = oracle.link_bytes_hier(0, 1, U, T, cu, True, Hq, Hkv, d, eb)
+    assert inter.shape[0] == 0
+    n = [128, 128, 127, 127]
+    hs, kvs = Hq // U, 1      # 2 query heads per slice, inside one key/value group of 4
+    for a in range(U):
+        for b in range(U):
+            want = 0 if a == b else n[a] * (hs + 2 * kvs) * d * eb + n[b] * hs * d * eb
+            assert intra[a, b] == want, (a, b)
+    R = 4
+    cu = np.array([0, 200, 512], dtype=np.int32)
+    intra, inter = oracle.link_bytes_hier(0, R, 1, 512, cu, True, Hq, Hkv, d, eb)
+    assert not intra.any()
+    flat = oracle.link_bytes(0, R, 512, cu, True, bytes_per_token=2 * Hkv * d * eb)
+    assert np.array_equal(inter, flat)

@@ -11,11 +11,14 @@ library. Every parameterisation of the oracle's pin tests then runs with the
 oracle module pointed at that library, and at least one of them must fail:
 all of test_oracle_pins.py, test_oracle_backward_pins.py and
 test_oracle_schedule_pins.py, and the test_oracle_* functions of
-test_chunking.py and test_comm_model.py (these call the oracle only, never
-the product). Mistakes are also planted in the chunk bounds (a balance bound
+test_chunking.py, test_comm_model.py and test_hier_schedule.py (these call
+the oracle only, never the product). Mistakes are also planted in the chunk bounds (a balance bound
 off by one, a causal row's work off by one, the document-snap threshold) and
 in the communication model (the ring's sender, the source walked forward, the
-needed-only look-ahead cut short, a TASP piece counted as a whole chunk).
+needed-only look-ahead cut short, a TASP piece counted as a whole chunk), and
+in the two-level check and model (a transposed rank layout, a wrong
+renumbering, the head range's end unchecked, the attention output sent the
+wrong way, another key/value-head map, K without V between groups).
 The unmodified oracle passes the same list (the control), so a failure means
 the pins caught the mistake, not that the harness broke."""
 import contextlib
@@ -30,6 +33,7 @@ import pytest
 import oracle
 import test_chunking
 import test_comm_model
+import test_hier_schedule
 import test_oracle_backward_pins
 import test_oracle_pins
 import test_oracle_schedule_pins
@@ -38,7 +42,7 @@ import test_oracle_schedule_pins
 # oracle alone (the chunking and communication modules also test the product).
 PIN_MODULES = [(test_oracle_pins, "test_"), (test_oracle_backward_pins, "test_"),
                (test_oracle_schedule_pins, "test_"), (test_chunking, "test_oracle_"),
-               (test_comm_model, "test_oracle_")]
+               (test_comm_model, "test_oracle_"), (test_hier_schedule, "test_oracle_")]
 
 # name -> (text in oracle.cpp, replacement); each text occurs exactly once.
 MUTANTS = {
@@ -102,6 +106,21 @@ MUTANTS = {
     "link_lookahead_short": ("          for (int k = 0; !keep && t + k <= P - 1; ++k)\n            if (wants((r + k) % P",
                              "          for (int k = 0; !keep && t + k < P - 1; ++k)\n            if (wants((r + k) % P"),
     "link_tasp_piece_as_chunk": ("                (kb - ka) * bytes_per_token;", "                (ce - cb) * bytes_per_token;"),
+    # Two-level schedules: the check and the communication model.
+    "hier_slice_of_rank_transposed": ("    const int u = r % U;\n    if (heads[2 * x]",
+                                      "    const int u = r / U;\n    if (heads[2 * x]"),
+    "hier_renumbering_wrong": ("    for (int c = 0; c < 8; ++c) slice[u].push_back(c == 0 ? r / U : it[c]);",
+                               "    for (int c = 0; c < 8; ++c) slice[u].push_back(c == 0 ? r % U : it[c]);"),
+    "hier_head_end_unchecked": ("    if (heads[2 * x] != u * hs || heads[2 * x + 1] != (u + 1) * hs)",
+                                "    if (heads[2 * x] != u * hs)"),
+    "hier_output_sent_the_wrong_way": (
+        "        intra[static_cast<size_t>(g * U + v) * P + owner] += static_cast<long long>(d) * eb;    // o",
+        "        intra[static_cast<size_t>(owner) * P + (g * U + v)] += static_cast<long long>(d) * eb;    // o"),
+    "hier_kv_heads_interleaved": ("  for (int h = 0; h < Hq; ++h) uses[h / hs][h / G] = 1;",
+                                  "  for (int h = 0; h < Hq; ++h) uses[h / hs][h % Hkv] = 1;"),
+    "hier_inter_bytes_k_only": (
+        "    const int rc = oracle_link_bytes(kind, R, T, cu, ndocs, causal, succ, 2 * nkv * d * eb, needed_only,",
+        "    const int rc = oracle_link_bytes(kind, R, T, cu, ndocs, causal, succ, nkv * d * eb, needed_only,"),
 }
 
 
