@@ -1,0 +1,34 @@
+"""The Python example in README.md runs as printed, and its outputs match the
+fp64 oracle on sampled rows (document edges, tile edges and random rows)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from gpu_util import TOL_BF16_LSE, TOL_BF16_O, max_errs, oracle_rows, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+README = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "README.md")
+
+
+def test_readme_python_example():
+    import torch
+    block = re.search(r"```python\n(.*?)```", open(README).read(), re.S).group(1)
+    torch.manual_seed(0)
+    ns = {}
+    exec(compile(block, "README.md", "exec"), ns)
+    q, k, v, o, lse, cu = ns["q"], ns["k"], ns["v"], ns["o"], ns["lse"], ns["cu"]
+    dq, dk, dv = ns["dq"], ns["dk"], ns["dv"]
+    T, Hq, d = q.shape
+    assert o.shape == q.shape and o.dtype == torch.bfloat16
+    assert lse.shape == (Hq, T) and lse.dtype == torch.float32
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+    assert all(bool(torch.isfinite(t.float()).all()) for t in (o, lse, dq, dk, dv))
+    rows = sample_rows(np.asarray(cu), T, [], n_random=48, seed=1)
+    o_ref, l_ref = oracle_rows(q, k, v, np.asarray(cu, dtype=np.int32), True, rows)
+    rows_t = torch.from_numpy(rows).cuda()
+    eo, el = max_errs(o[rows_t].float().cpu().numpy().astype(np.float64),
+                      lse[:, rows_t].t().cpu().numpy().astype(np.float64), o_ref, l_ref)
+    assert eo <= TOL_BF16_O and el <= TOL_BF16_LSE, (eo, el)
