@@ -118,6 +118,10 @@ MUTANTS = {
         "        intra[static_cast<size_t>(owner) * P + (g * U + v)] += static_cast<long long>(d) * eb;    // o"),
     "hier_kv_heads_interleaved": ("  for (int h = 0; h < Hq; ++h) uses[h / hs][h / G] = 1;",
                                   "  for (int h = 0; h < Hq; ++h) uses[h / hs][h % Hkv] = 1;"),
+    # Packing descriptor.
+    "cu_seqlens_empty_document_accepted": ("    if (cu[i + 1] <= cu[i]) return 2;", "    if (cu[i + 1] < cu[i]) return 2;"),
+    "doc_of_boundary_off_by_one": ("    if (cu[mid] <= t) lo = mid; else hi = mid - 1;",
+                                   "    if (cu[mid] < t) lo = mid; else hi = mid - 1;"),
     "hier_inter_bytes_k_only": (
         "    const int rc = oracle_link_bytes(kind, R, T, cu, ndocs, causal, succ, 2 * nkv * d * eb, needed_only,",
         "    const int rc = oracle_link_bytes(kind, R, T, cu, ndocs, causal, succ, nkv * d * eb, needed_only,"),
