@@ -232,8 +232,11 @@ sp_status sp_partial_attn(const void* q, const void* k, const void* v, float* o_
                           const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal, float scale,
                           void* stream);
 
-/* sp_lse_merge — folds one normalised partial into an accumulator, in place,
- * by the log-sum-exp rule (exact for partials over disjoint key sets):
+/* sp_lse_merge — folds one normalised partial into an accumulator, in place:
+ * the step that combines the results of "partial attention computation"
+ * (HSAP abstract) across the iterations of a Ring Attention schedule (TASP
+ * abstract). The pages name no formula; the rule is the log-sum-exp merge,
+ * exact for partials over disjoint key sets:
  *   M = max(L1, L2), L = M + log(exp(L1 - M) + exp(L2 - M)),
  *   O = exp(L1 - L) O1 + exp(L2 - L) O2.
  * A partial with L = -inf is the identity; two -inf stay -inf with O = 0.
