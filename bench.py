@@ -588,8 +588,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="seconds of oracle work for the cpu_baseline field")
+    ap.add_argument("--cpu-seconds", type=float, default=None,
+                    help="seconds of oracle work for the cpu_baseline field (default 12); with "
+                         "--impl reference, per timed step (default: 120 s over all steps, 1-20 s each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward measurement reported beside the headline")
@@ -611,7 +612,8 @@ def main():
     if args.impl == "reference":
         # The fp64 CPU oracle on a bounded sample per step, rank 0 only.
         if rank == 0:
-            per_step = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+            per_step = (args.cpu_seconds if args.cpu_seconds is not None else
+                        max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup))))
             for _ in range(args.warmup):
                 oracle_sample(w, cu, per_step * 0.25, seed=99)
             flop = elapsed = rows = 0
@@ -651,7 +653,7 @@ def main():
         if args.no_cpu_baseline or world > 1:
             result["cpu_baseline"] = None
         else:
-            f, e, n, threads = oracle_sample(w, cu, args.cpu_seconds)
+            f, e, n, threads = oracle_sample(w, cu, args.cpu_seconds if args.cpu_seconds is not None else 12.0)
             rate = f / e  # oracle FLOP/s over valid pairs
             result["cpu_baseline"] = {
                 "value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
