@@ -373,9 +373,14 @@ extern "C" sp_status sp_packed_attention_static_ws(const void* q, const void* k,
                                                    int32_t causal, float scale,
                                                    const sp_item* items_dev, int64_t n_items,
                                                    void* stream) {
+  // Argument errors are returned before any CUDA call, as by sp_packed_attention.
+  const sp_status s = check_shapes(T, Hq, Hkv, d, dtype, ndocs, scale);
+  if (s != SP_OK) return s;
+  if (n_items < 0) return SP_ERR_INVALID_ARG;
   if (n_items > SP_STATIC_WS_MAX_ITEMS ||
       sp_packed_attention_workspace_size(n_items) > SP_STATIC_WS_BYTES)
     return SP_ERR_BUFFER_TOO_SMALL;
+  if (T == 0 || n_items == 0) return SP_OK;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SP_ERR_CUDA;
   void* ws = nullptr;

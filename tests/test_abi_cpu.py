@@ -145,3 +145,35 @@ def test_backward_argument_checks():
     assert bwd(items=None) == 1
     base = sb.sp_packed_attention_workspace_size(10)
     assert sb.sp_packed_attention_backward_workspace_size(10, 512, 4) >= base + 512 * 4 * 4
+
+
+def test_packed_ex_and_static_ws_argument_checks():
+    lib = sb.load()
+    max_items = int(re.search(r"#define SP_STATIC_WS_MAX_ITEMS (\d+)", open(HEADER).read()).group(1))
+    base = dict(T=512, Hq=4, Hkv=4, d=128, dtype=0, nd=1, causal=1, scale=0.1)
+
+    def ex(n_items=10, ws_bytes=None, q=FAKE, heads=FAKE, **kw):
+        ws = sb.sp_packed_attention_workspace_size(n_items) if ws_bytes is None else ws_bytes
+        a = dict(base, **kw)
+        return lib.sp_packed_attention_ex(q, FAKE, FAKE, FAKE, FAKE, a["T"], a["Hq"], a["Hkv"], a["d"],
+                                          a["dtype"], FAKE, a["nd"], a["causal"], a["scale"], FAKE, heads,
+                                          n_items, FAKE, ws, None)
+
+    assert ex(n_items=-1) == 1
+    assert ex(n_items=0) == 0 and ex(T=0) == 0
+    assert ex(q=None) == 1
+    assert ex(q=ctypes.c_void_p(0x100008)) == 1        # device pointers: 16-byte aligned
+    assert ex(heads=ctypes.c_void_p(0x100004)) == 1    # head ranges: int32 pairs, 8-byte aligned
+    assert ex(d=32) == 2 and ex(Hq=6, Hkv=4) == 1 and ex(scale=float("inf")) == 1
+    assert ex(ws_bytes=16) == 3
+
+    def static(n_items=10, **kw):
+        a = dict(base, **kw)
+        return lib.sp_packed_attention_static_ws(FAKE, FAKE, FAKE, FAKE, FAKE, a["T"], a["Hq"], a["Hkv"],
+                                                 a["d"], a["dtype"], FAKE, a["nd"], a["causal"], a["scale"],
+                                                 FAKE, n_items, None)
+
+    assert static(n_items=max_items + 1) == 3
+    assert static(d=32) == 2 and static(scale=0.0) == 1 and static(Hq=3, Hkv=2) == 1
+    assert static(n_items=-1) == 1
+    assert static(n_items=0) == 0 and static(T=0) == 0
