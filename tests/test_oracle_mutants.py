@@ -73,6 +73,16 @@ MUTANTS = {
     "dp_from_keys": ("          for (int c = 0; c < d; ++c) dp += doi[c] * widen(v, dtype, kb + c);",
                      "          for (int c = 0; c < d; ++c) dp += doi[c] * widen(k, dtype, kb + c);"),
     "sampled_dp_is_the_score": ("  *dp = dpd;", "  *dp = dot;"),
+    "sampled_key_queries_skip_diagonal": (
+        "        for (int i = causal ? j : cu[D]; i < cu[D + 1]; ++i) {\n          const RowStats& st",
+        "        for (int i = causal ? j + 1 : cu[D]; i < cu[D + 1]; ++i) {\n          const RowStats& st"),
+    "sampled_dq_keys_skip_diagonal": (
+        "      const int j1 = causal ? std::min(cu[D + 1], i + 1) : cu[D + 1];\n      double* out = dq_rows",
+        "      const int j1 = causal ? std::min(cu[D + 1], i) : cu[D + 1];\n      double* out = dq_rows"),
+    "sampled_heads_of_kv_interleaved": ("      for (int h = g * G; h < (g + 1) * G; ++h)\n        for (int i = causal ? j : cu[D]",
+                                        "      for (int h = g; h < Hq; h += Hkv)\n        for (int i = causal ? j : cu[D]"),
+    "row_stats_D_from_queries": ("  for (int c = 0; c < d; ++c) r.D += widen(dout, dtype, qb + c) * o[c];",
+                                 "  for (int c = 0; c < d; ++c) r.D += widen(q, dtype, qb + c) * o[c];"),
     "valid_pairs_causal_off_by_one": ("      const int hi = std::min(c1, i + 1);\n      if (hi > c0)",
                                       "      const int hi = std::min(c1, i);\n      if (hi > c0)"),
     # Schedules: the closed forms and the checks.
