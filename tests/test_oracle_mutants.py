@@ -58,6 +58,10 @@ MUTANTS = {
                             "      const double lse = std::log(sum);\n      std::fill(acc"),
     "values_read_from_keys": ("        for (int c = 0; c < d; ++c) acc[c] += w * widen(v, dtype, vb + c);",
                               "        for (int c = 0; c < d; ++c) acc[c] += w * widen(k, dtype, vb + c);"),
+    "partial_range_end_inclusive": ("      int j1 = std::min(cu[D + 1], kv_end);",
+                                    "      int j1 = std::min(cu[D + 1], kv_end + 1);"),
+    "row_without_keys_gets_lse_zero": ("        lse_out[static_cast<size_t>(r) * Hq + h] = NEG_INF;\n        continue;",
+                                       "        lse_out[static_cast<size_t>(r) * Hq + h] = 0.0;\n        continue;"),
     "merge_weight_offset": ("    const double wa = std::exp(a - L), wb = std::exp(b - L);",
                             "    const double wa = std::exp(a - M), wb = std::exp(b - L);"),
     "ds_sign_flipped": ("          const double ds = pij * (dp - Di);",
