@@ -351,8 +351,8 @@ def run_ours(args, world, rank, local):
         bflop = 2.5 * flop  # QK^T and dO V^T recomputed, dV, dK, dQ: 10 d per pair and head
         bwd = {"ms_per_call": round(b_ms, 4), "tflops": round(bflop / (b_ms * 1e-3) / 1e12, 2),
                "flop_per_call": bflop, "flop_convention": "10*d*Hq*valid_pairs (2.5x forward)",
-               "frac_of_peak": None, "launches_per_call": 4,
-               "kernels": "bwd_rowdot, prep_kernel, bwd_dq_kernel<128>, bwd_dkdv_kernel<128>"}
+               "frac_of_peak": None, "launches_per_call": 3,
+               "kernels": "bwd_rowdot_kernel, bwd_fused_kernel<128>, bwd_dq_convert_kernel"}
         del dout, dq, dk, dv
 
     # ---- secondary: the log-sum-exp merge kernel of the unfused API path,

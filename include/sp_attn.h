@@ -322,7 +322,9 @@ sp_status sp_packed_attention_static_ws(const void* q, const void* k, const void
                                         float scale, const sp_item* items_dev, int64_t n_items,
                                         void* stream);
 
-/* Bytes of device workspace sp_packed_attention_backward needs. */
+/* Bytes of device workspace sp_packed_attention_backward needs: a small
+ * header, two fp32 [Hq][T] row vectors and an fp32 [T][Hq][128] dQ
+ * accumulator (n_items does not change it). */
 size_t sp_packed_attention_backward_workspace_size(int64_t n_items, int32_t T, int32_t Hq);
 
 /* sp_packed_attention_backward — gradients of sp_packed_attention for
@@ -337,11 +339,14 @@ size_t sp_packed_attention_backward_workspace_size(int64_t n_items, int32_t T, i
  *     forward's outputs for the same inputs; dout has the layout of o).
  *  lse: device float32 [Hq][T], natural log, as the forward wrote it.
  *  dq: device bf16 [T][Hq][d]; dk, dv: device bf16 [T][Hkv][d]; every element
- *     is written (keys no query attends get 0).
+ *     is written (keys no query attends and queries without keys get 0).
  *  items_dev: a complete schedule (every pair the mask allows exactly once,
- *     as sp_schedule_build produces). dQ walks the items like the forward;
- *     dK and dV are accumulated key-tile by key-tile over the pairs the mask
- *     allows, which for a complete schedule is the same set.
+ *     as sp_schedule_build produces). The gradients are sums over the pairs
+ *     the mask allows, which for a complete schedule are the pairs its items
+ *     hold; they are accumulated key tile by key tile, so the items fix only
+ *     the order of the sums and are not read (n_items must still be >= 1).
+ *  dK and dV are bit-reproducible from run to run; dQ is summed with fp32
+ *     reductions in global memory whose order varies, so its low bits may.
  *  dtype must be SP_DTYPE_BF16 (SP_ERR_UNSUPPORTED otherwise); d is 64 or 128.
  *  workspace: device, at least sp_packed_attention_backward_workspace_size
  *     bytes, owned by the caller; calls sharing it must not overlap in time.

@@ -10,35 +10,46 @@
 // second; TASP abstract: Ring Attention and its decompositions).
 //
 // Three kernels, launched in order on one stream:
-//   bwd_rowdot   -scale D_i and -LSE_i log2(e) per (row, head) into the workspace.
-//   bwd_dkdv     one unit per (key/value head, 128-key tile), head-major so
-//                that the CTAs running at one time share the Q and dO of one
-//                head group in L2. K and V stay in shared memory while every
-//                128-row Q tile that can attend the keys streams through (all
-//                query heads of the group). Keys sit on the tensor-memory
-//                lanes: S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
-//                dK += dS^T Q with P^T and dS^T read from tensor memory.
-//   bwd_dq       one unit per (128-row Q tile, query head), walking the same
-//                schedule items as the forward in 128-key tiles: S = Q K^T,
-//                dP = dO V^T, dQ += dS K with dS read from tensor memory.
-// Every MMA is 128 x 128 x 16 (a 128 x 64 MMA costs as long as a 128 x 128
-// one, so narrower steps would halve the tensor-core rate). The elementwise
-// work of a step is split by columns between two compute warpgroups (64
-// columns each, P kept in registers between the S and the dP phase), and the
-// MMA lane interleaves (dV or nothing)(g), S(g+1), (dK or dQ)(g), dP(g+1):
-// S(g+1) runs while the warpgroups turn dP(g) into dS(g), and dK/dQ(g) and
-// dP(g+1) run while they turn S(g+1) into P. Each kernel: warp 0 TMA
-// producer, warp 1 TMEM owner and MMA lane, warps 4-11 two compute
-// warpgroups (one TMEM lane, i.e. one key or query row, per thread). Tensor maps use {64 dims, 1 head, 64 rows}
-// boxes with 128-byte swizzle; a 128-row tile is two boxes, row r at r x 128
-// bytes of each 64-dim sub-tile, the layout one 128-row box would give.
+//   bwd_rowdot     -scale D_i and -LSE_i log2(e) per (row, head) into the
+//                  workspace; zeroes the fp32 dQ accumulator and the unit queue.
+//   bwd_fused      one unit per (key/value head, 128-key tile), head-major so
+//                  that the CTAs running at one time share the Q, dO and dQ
+//                  accumulator rows of one head group in L2. K and V stay in
+//                  shared memory while every 128-row Q tile that can attend the
+//                  keys streams through (all query heads of the group). Keys
+//                  sit on the tensor-memory lanes: S^T = K Q^T, dP^T = V dO^T,
+//                  dV += P^T dO and dK += dS^T Q with P^T and dS^T read from
+//                  tensor memory; dS also goes to shared memory, where it is
+//                  the B operand of the step's dQ tile, dQ^T = K^T dS^T
+//                  (d on the tensor-memory lanes, queries on the columns). The
+//                  tile is added into an fp32 accumulator with reductions in
+//                  which each warp covers 32 consecutive floats of one query's
+//                  row (one 128-byte line); they are spread over the next
+//                  step's phases because the L2 accepts reductions at a
+//                  bounded rate (about 6 TB/s measured on this GPU).
+//                  Each S and dP is computed once: 10 d FLOP of tensor work per
+//                  valid (query, key) pair and query head.
+//   bwd_dq_convert the accumulator rounded to bf16 into dQ.
+// Every MMA is 128 x 128 x 16 or 128 x d x 16 (a 128 x 64 MMA costs as long
+// as a 128 x 128 one, so narrower steps would halve the tensor-core rate). The
+// elementwise work of a step is split by columns between two compute
+// warpgroups (64 columns each, P kept in registers between the S and the dP
+// phase). Per step g the MMA lane issues dK(g), dQ(g), dV(g+1), dP(g+1),
+// S(g+2): dV(g+1) fills the time the compute warps take to read dQ(g) out of
+// the tensor-memory columns dP(g+1) reuses, and S(g+2) runs while they turn
+// dP(g+1) into dS. The fp32 reductions make dQ's summation order vary from run
+// to run (dK and dV are summed in a fixed order). Roles: warp 0 TMA producer, warp 1 TMEM owner and MMA
+// lane, warps 4-11 two compute warpgroups (one TMEM lane, i.e. one key or
+// query row, per thread). Tensor maps use {64 dims, 1 head, 64 rows} boxes
+// with 128-byte swizzle; a 128-row tile is two boxes, row r at r x 128 bytes
+// of each 64-dim sub-tile, the layout one 128-row box would give.
 
 #include <cuda.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "sp_device.cuh"
-#include "sp_tiles.cuh"
 
 namespace sp {
 namespace {
@@ -53,13 +64,14 @@ struct BCfg {
   static constexpr int TILE = KSUB * SUB;    // bytes of a 128-row tile
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // both K-major
   static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, 0, 1);  // B MN-major
+  static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D == 128 ? 128 : D, 1, 1);  // A, B MN-major
   static constexpr int TMEM_COLS = 512;
 };
 
 // K-major operand descriptor (rows = M or N, 64 dims per 128-byte row).
 __device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return smem_desc_sw128(addr, 16, 1024); }
-// MN-major B operand over a 128-row tile: the next 64 columns of N start one
-// sub-tile further on.
+// MN-major operand over a 128-row tile: the next 64 columns of M or N start
+// one sub-tile further on.
 __device__ __forceinline__ uint64_t desc_mn(uint32_t addr) { return smem_desc_sw128(addr, 128 * 128, 1024); }
 
 // D/16 MMAs contracting over d: C[128 x 128] = A B^T, A and B 128-row K-major tiles.
@@ -87,6 +99,26 @@ __device__ __forceinline__ void mma_acc(uint32_t d_t, uint32_t a_t, uint32_t b_a
   for (int kk = 0; kk < 8; ++kk)
     tc_mma_ts(d_t, a_t + 8 * kk + (kk >= 4 ? 32 : 0), b0 + static_cast<uint64_t>(kk * (2048 >> 4)),
               C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
+}
+
+// 8 MMAs contracting over the 128 keys of a tile. dS sits in shared memory
+// as [key][query] (two 64-query sub-tiles, query-major); K is the key tile
+// ([key][d], d-major).
+// d = 128: dQ_tile^T[d x 128 queries] = K^T dS^T (A = K, B = dS), so that the
+//   tensor-memory lanes are the head dimension and a warp's 32 lanes hold 32
+//   consecutive floats of one query's accumulator row.
+// d = 64: dQ_tile[128 queries x d] = dS K (a 64-row MMA would change the
+//   tensor-memory layout; this head dimension is not on the fast path).
+template <int D>
+__device__ __forceinline__ void mma_dq(uint32_t d_t, uint32_t ds_addr, uint32_t k_addr) {
+  using C = BCfg<D>;
+  const uint64_t ds0 = desc_mn(ds_addr), k0 = desc_mn(k_addr);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t o = static_cast<uint64_t>(kk * (2048 >> 4));
+    if (D == 128) tc_mma_ss(d_t, k0 + o, ds0 + o, C::IDESC_DQ, kk > 0 ? 1u : 0u);
+    else tc_mma_ss(d_t, ds0 + o, k0 + o, C::IDESC_DQ, kk > 0 ? 1u : 0u);
+  }
 }
 
 // TMA of a 128-row block as two 64-row boxes into a 128-row tile (row0 < T).
@@ -117,6 +149,22 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Adds four consecutive fp32 values into global memory (p 16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "f"(__uint_as_float(a)), "f"(__uint_as_float(b)), "f"(__uint_as_float(c)),
+                  "f"(__uint_as_float(d))
+               : "memory");
+}
+__device__ __forceinline__ void red_add(float* p, uint32_t a) {
+  asm volatile("red.global.add.f32 [%0], %1;" :: "l"(p), "f"(__uint_as_float(a)) : "memory");
+}
+
 // Writes 32 fp32 accumulator columns of one row as bf16.
 __device__ __forceinline__ void store_row32_bf16(uint16_t* dst, const uint32_t (&rr)[32]) {
 #pragma unroll
@@ -133,9 +181,6 @@ __device__ __forceinline__ void store_row32_bf16(uint16_t* dst, const uint32_t (
 __device__ __forceinline__ void store_zero_row_bf16(uint16_t* dst, int n) {
   for (int j = 0; j < n; j += 8) *reinterpret_cast<uint4*>(dst + j) = make_uint4(0, 0, 0, 0);
 }
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Loads 64 consecutive TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld64(uint32_t t, uint32_t (&x)[64]) {
@@ -154,9 +199,8 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
-// Per-column values of a step (one per query column, staged in shared memory)
-// or one per-row value broadcast to every column; pair4(c) gives the pairs
-// for columns (c, c+1) and (c+2, c+3).
+// Per-column values of a step (one per query column, staged in shared memory);
+// pair4(c) gives the pairs for columns (c, c+1) and (c+2, c+3).
 struct ColVals {
   const float* v;
   __device__ __forceinline__ void pair4(int c, uint64_t& p01, uint64_t& p23) const {
@@ -165,17 +209,13 @@ struct ColVals {
     p23 = f2_pack(q.z, q.w);
   }
 };
-struct RowVal {
-  uint64_t v2;
-  __device__ __forceinline__ void pair4(int, uint64_t& p01, uint64_t& p23) const { p01 = p23 = v2; }
-};
 
 // One compute warpgroup's half of a step (64 of the 128 columns, starting
 // at column c0 of the operand): given S of those columns in p[], replaces it
 // by P = 2^(S sl2 + nlse2) with nlse2 = -LSE log2 e on columns [lo, hi) (0
 // elsewhere), in fp32.
-template <bool kMask, typename Src>
-__device__ __forceinline__ void p_half_impl(int c0, int lo, int hi, float sl2, Src nlse2, uint32_t (&p)[64]) {
+template <bool kMask>
+__device__ __forceinline__ void p_half_impl(int c0, int lo, int hi, float sl2, ColVals nlse2, uint32_t (&p)[64]) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
   for (int c = 0; c < 64; c += 4) {
@@ -203,8 +243,7 @@ __device__ __forceinline__ void p_half_impl(int c0, int lo, int hi, float sl2, S
 
 // The mask is skipped when no lane of the warp needs it for these columns
 // (the tensor-memory accesses must stay warp-uniform).
-template <typename Src>
-__device__ __forceinline__ void p_half(int c0, int lo, int hi, float sl2, Src nlse2, uint32_t (&p)[64]) {
+__device__ __forceinline__ void p_half(int c0, int lo, int hi, float sl2, ColVals nlse2, uint32_t (&p)[64]) {
   if (__all_sync(0xffffffffu, lo <= c0 && hi >= c0 + 64)) p_half_impl<false>(c0, lo, hi, sl2, nlse2, p);
   else p_half_impl<true>(c0, lo, hi, sl2, nlse2, p);
 }
@@ -218,11 +257,17 @@ __device__ __forceinline__ void store_pairs32(uint32_t dst, const uint32_t (&v)[
 }
 
 // dS = P (dP scale + ndsc) with ndsc = -D scale, i.e. P (dP - D) scale, for
-// the same 64 columns (dP at t_dp, column c0 of the operand), written as 32
-// bf16-pair columns at t_dp: chunk h of 32 dP columns writes packed columns
-// 16h .. 16h+15, which chunk 0 has already read.
-template <typename Src>
-__device__ __forceinline__ void ds_half(uint32_t t_dp, int c0, const uint32_t (&p)[64], float scale, Src ndsc) {
+// the same 64 columns (dP at t_dp, column c0 of the operand), rounded to bf16
+// pairs and written twice: over the first 32 of those tensor-memory columns
+// (the A operand of dK += dS^T Q), and as this thread's 128-byte row of its
+// warpgroup's 64-query sub-tile of dS in shared memory (the A operand of the
+// dQ MMA), with the 128-byte swizzle: 16-byte chunk c of row r at chunk
+// c ^ (r mod 8). Done in two halves of 32 columns (half hh writes packed
+// columns 16hh .. 16hh+15, which half 0 has already read); between them
+// mid() runs (the caller's other work).
+template <typename Mid>
+__device__ __forceinline__ void ds_half(uint32_t t_dp, int c0, const uint32_t (&p)[64], float scale,
+                                        ColVals ndsc, uint32_t ds_row, uint32_t r7, Mid&& mid) {
   const uint64_t sc2 = f2_pack(scale, scale);
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
@@ -245,6 +290,11 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, int c0, const uint32_t (&
       pk[(c >> 1) + 1] = pack_bf16x2(s2, s3);
     }
     tmem_st16(t_dp + 16 * hh, pk);
+#pragma unroll
+    for (uint32_t ch = 0; ch < 4; ++ch)
+      st_shared_v4(ds_row + (((4 * hh + ch) ^ r7) << 4), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                   pk[4 * ch + 3]);
+    if (hh == 0) mid();
   }
 }
 
@@ -252,13 +302,17 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, int c0, const uint32_t (&
 
 // ndsc[h][t] = -scale * (dO[t][h][:] . O[t][h][:]) in fp32 from bf16, and
 // nlse2[h][t] = -lse[h][t] * log2(e); one warp per (t, h). The signs and the
-// scale are folded in so that the tensor-core kernels need one FMA per value.
+// scale are folded in so that the tensor-core kernel needs one FMA per value.
+// Also zeroes the (t, h) row of the fp32 dQ accumulator [T][Hq][d] and the
+// fused kernel's unit counter, which the next kernel on the stream reads.
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restrict__ o,
                                                          const uint16_t* __restrict__ dout,
                                                          const float* __restrict__ lse,
                                                          float* __restrict__ ndsc, float* __restrict__ nlse2,
+                                                         float* __restrict__ dqacc, int32_t* unit_counter,
                                                          int T, int Hq, int d, float scale) {
   const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *unit_counter = 0;
   const long long n = static_cast<long long>(T) * Hq;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -273,6 +327,8 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restr
       acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
       acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
     }
+    float4* zq = reinterpret_cast<float4*>(dqacc + static_cast<size_t>(w) * d);
+    for (int c = lane; c < d / 4; c += 32) zq[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
@@ -283,26 +339,53 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restr
   }
 }
 
-// ------------------------------------------------------------------ dK, dV
+// dq = bf16(acc), 8 elements per thread and pass (n8 = elements / 8).
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ acc,
+                                                             uint16_t* __restrict__ dq, long long n8) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
+    const float4 y = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+    uint4 w;
+    w.x = pack_bf16x2(x.x, x.y);
+    w.y = pack_bf16x2(x.z, x.w);
+    w.z = pack_bf16x2(y.x, y.y);
+    w.w = pack_bf16x2(y.z, y.w);
+    reinterpret_cast<uint4*>(dq)[i] = w;
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV, dQ
 
 template <int D>
-struct KVCfg : BCfg<D> {
+struct FCfg : BCfg<D> {
   using B = BCfg<D>;
   static constexpr int QSTAGE = 2;
-  static constexpr int STAGE_BYTES = 2 * B::TILE + 1024;  // Q, dO, LSE2[128], D[128]
+  static constexpr int STAGE_BYTES = 2 * B::TILE + 1024;  // Q, dO, -LSE log2 e [128], -scale D [128]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = B::TILE;
-  static constexpr int OFF_QD = 2 * B::TILE;
+  static constexpr int OFF_DS = 2 * B::TILE;  // dS [128 keys][128 queries] bf16: two 64-query sub-tiles
+  static constexpr int OFF_QD = OFF_DS + 2 * B::SUB;
   static constexpr int OFF_BAR = OFF_QD + QSTAGE * STAGE_BYTES;
-  static constexpr int N_BARS = 17;
+  static constexpr int N_BARS = 19;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;  // TMEM address, abort flag, unit ring[2]
-  static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+  // The dynamic shared memory base is 1024-byte aligned on this GPU (the
+  // kernel checks it), so the layout needs no slack for realignment: at
+  // d = 128 it takes 231,600 of the 232,448 bytes a block may have.
+  static constexpr int SMEM_ALLOC = OFF_MISC + 16;
+  // Tensor memory: S^T (P^T as bf16 over its columns 0-31 and 64-95), dP^T
+  // (then dS^T the same way), dV, dK. The dQ tile of a step takes the dP^T
+  // columns at d = 128 (free once dS^T has been read by dK; lanes = d, columns
+  // = queries) and columns of its own at d = 64 (lanes = queries).
   static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
+  static constexpr int TM_DQ = D == 128 ? TM_DP : 256 + 2 * D;
+  static constexpr int DQ_COLS = 64 * D / 128;  // dQ tile columns per compute warpgroup
 };
+static_assert(FCfg<128>::SMEM_ALLOC <= 232448, "fused backward layout exceeds the shared memory of a block");
 
-enum { KB_KV_FULL = 0, KB_KV_EMPTY = 1, KB_QD_FULL = 2, KB_QD_EMPTY = 4, KB_S_FULL = 6, KB_DP_FULL = 7,
-       KB_P_FULL = 8, KB_DS_FULL = 9, KB_ACC_FULL = 10, KB_ACC_EMPTY = 11, KB_DRAIN = 12, KB_U_FULL = 13,
-       KB_U_EMPTY = 15 };
+enum { FB_KV_FULL = 0, FB_KV_EMPTY = 1, FB_QD_FULL = 2, FB_QD_EMPTY = 4, FB_S_FULL = 6, FB_DP_FULL = 7,
+       FB_P_FULL = 8, FB_DS_FULL = 9, FB_DQ_FULL = 10, FB_DQ_READ = 11, FB_ACC_FULL = 12,
+       FB_ACC_EMPTY = 13, FB_DRAIN = 14, FB_U_FULL = 15, FB_U_EMPTY = 17 };
 constexpr int KV_UNIT_CONSUMERS = 9;  // the MMA lane and the eight compute warps
 
 struct KVUnit {
@@ -313,7 +396,8 @@ struct KVUnit {
 
 // Units are head-major: all key tiles of head 0, then head 1, ...; within a
 // head the key tiles in order, which for causal masks is longest first. CTAs
-// claim units from an atomic counter in that order.
+// claim units from an atomic counter in that order. Step n of a unit is query
+// head hk G + n mod G over the Q tile at qa + 128 (n / G).
 __device__ __forceinline__ KVUnit kv_unit(const AttnArgs& a, int u) {
   KVUnit w;
   const int n_tiles = (a.T + 127) / 128;
@@ -331,15 +415,19 @@ __device__ __forceinline__ KVUnit kv_unit(const AttnArgs& a, int u) {
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
-bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
-                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                const __grid_constant__ CUtensorMap tmdo) {
-  using C = KVCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+bwd_fused_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
+                 const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                 const __grid_constant__ CUtensorMap tmdo) {
+  using C = FCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sQD = sbase + C::OFF_QD;
+  const AttnArgs& f = a.fwd;
+  if (sbase & 1023u) {  // the layout has no slack to realign (see FCfg)
+    if (threadIdx.x == 0) atomicOr(f.err, ERR_INTERNAL_BIT);
+    return;
+  }
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
+  const uint32_t sQD = sbase + C::OFF_QD;
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -347,26 +435,27 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   volatile int* uring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const AttnArgs& f = a.fwd;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(KB_KV_FULL), 1);
-    mbar_init(bar(KB_KV_EMPTY), 1);
+    mbar_init(bar(FB_KV_FULL), 1);
+    mbar_init(bar(FB_KV_EMPTY), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(KB_U_FULL + s), 1);
-      mbar_init(bar(KB_U_EMPTY + s), KV_UNIT_CONSUMERS);
+      mbar_init(bar(FB_U_FULL + s), 1);
+      mbar_init(bar(FB_U_EMPTY + s), KV_UNIT_CONSUMERS);
     }
     for (int s = 0; s < C::QSTAGE; ++s) {
-      mbar_init(bar(KB_QD_FULL + s), 32);  // one asynchronous arrival per producer lane
-      mbar_init(bar(KB_QD_EMPTY + s), 1);
+      mbar_init(bar(FB_QD_FULL + s), 32);  // one asynchronous arrival per producer lane
+      mbar_init(bar(FB_QD_EMPTY + s), 1);
     }
-    mbar_init(bar(KB_S_FULL), 1);
-    mbar_init(bar(KB_DP_FULL), 1);
-    mbar_init(bar(KB_P_FULL), 8);   // both compute warpgroups, one arrival per warp
-    mbar_init(bar(KB_DS_FULL), 8);
-    mbar_init(bar(KB_ACC_FULL), 1);
-    mbar_init(bar(KB_ACC_EMPTY), 8);
-    mbar_init(bar(KB_DRAIN), 1);
+    mbar_init(bar(FB_S_FULL), 1);
+    mbar_init(bar(FB_DP_FULL), 1);
+    mbar_init(bar(FB_P_FULL), 8);   // both compute warpgroups, one arrival per warp
+    mbar_init(bar(FB_DS_FULL), 8);
+    mbar_init(bar(FB_DQ_FULL), 1);
+    mbar_init(bar(FB_DQ_READ), 8);
+    mbar_init(bar(FB_ACC_FULL), 1);
+    mbar_init(bar(FB_ACC_EMPTY), 8);
+    mbar_init(bar(FB_DRAIN), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -381,6 +470,10 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   const int G = f.Hq / f.Hkv;
   const int n_units = ((f.T + 127) / 128) * f.Hkv;
   const unsigned long long tmo = f.timeout_ns;
+  // Registers: the block is launched with 384 x 168; the producer/MMA
+  // warpgroup gives up 48 per thread to the two compute warpgroups
+  // (4 x 32 x 120 + 8 x 32 x 192 = 384 x 168).
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 120;");
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -397,10 +490,10 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       if (lane == 0) {
         u = atomicAdd(a.unit_counter, 1);
         if (u >= n_units) u = -1;
-        pub = mbar_wait_bounded(bar(KB_U_EMPTY + uslot), uph ^ 1, tmo, f.err, abort_flag);
+        pub = mbar_wait_bounded(bar(FB_U_EMPTY + uslot), uph ^ 1, tmo, f.err, abort_flag);
         if (pub) {
           uring[uslot] = u;
-          mbar_arrive(bar(KB_U_FULL + uslot));
+          mbar_arrive(bar(FB_U_FULL + uslot));
         }
       }
       u = __shfl_sync(0xffffffffu, u, 0);
@@ -410,13 +503,13 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       const KVUnit w = kv_unit(f, u);
       bool got = true;
       if (lane == 0) {
-        got = mbar_wait_bounded(bar(KB_KV_EMPTY), (unit_cnt & 1) ^ 1, tmo, f.err, abort_flag);
+        got = mbar_wait_bounded(bar(FB_KV_EMPTY), (unit_cnt & 1) ^ 1, tmo, f.err, abort_flag);
         if (got) {
-          mbar_arrive_expect_tx(bar(KB_KV_FULL), 2 * C::TILE);
+          mbar_arrive_expect_tx(bar(FB_KV_FULL), 2 * C::TILE);
           armed_kv = 1;
           par_kv = unit_cnt & 1;
-          load_rows128<D>(sK, &tmk, bar(KB_KV_FULL), w.hk, w.k0, f.T);
-          load_rows128<D>(sV, &tmv, bar(KB_KV_FULL), w.hk, w.k0, f.T);
+          load_rows128<D>(sK, &tmk, bar(FB_KV_FULL), w.hk, w.k0, f.T);
+          load_rows128<D>(sV, &tmv, bar(FB_KV_FULL), w.hk, w.k0, f.T);
         }
       }
       if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) { ok = false; break; }
@@ -425,9 +518,9 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         const uint32_t ph = (gs / C::QSTAGE) & 1;
         const int h = w.hk * G + step % G;
         const int q0 = w.qa + 128 * (step / G);
-        const bool e = mbar_wait_bounded(bar(KB_QD_EMPTY + st), ph ^ 1, tmo, f.err, abort_flag);
+        const bool e = mbar_wait_bounded(bar(FB_QD_EMPTY + st), ph ^ 1, tmo, f.err, abort_flag);
         if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-        const uint32_t full = bar(KB_QD_FULL + st);
+        const uint32_t full = bar(FB_QD_FULL + st);
         const uint32_t sq = sQD + st * C::STAGE_BYTES;
         if (lane == 0) {
           mbar_expect_tx(full, 2 * C::TILE);
@@ -446,12 +539,13 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         }
         cp_async_arrive(full);
       }
+      if (!ok) break;
     }
     if (!ok && lane == 0) {
       volatile int no_abort = 0;
-      if (armed_kv) mbar_wait_bounded(bar(KB_KV_FULL), par_kv, 50000000ull, f.err, &no_abort);
+      if (armed_kv) mbar_wait_bounded(bar(FB_KV_FULL), par_kv, 50000000ull, f.err, &no_abort);
       for (int s = 0; s < C::QSTAGE; ++s)
-        if (armed_qd[s]) mbar_wait_bounded(bar(KB_QD_FULL + s), par_qd[s], 50000000ull, f.err, &no_abort);
+        if (armed_qd[s]) mbar_wait_bounded(bar(FB_QD_FULL + s), par_qd[s], 50000000ull, f.err, &no_abort);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
@@ -459,91 +553,112 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
     // ------------------------------------------------------------ MMA lane
     if (lane == 0) {
       const uint32_t tS = tmem + C::TM_S, tdP = tmem + C::TM_DP;
-      const uint32_t tdV = tmem + C::TM_DV, tdK = tmem + C::TM_DK;
+      const uint32_t tdV = tmem + C::TM_DV, tdK = tmem + C::TM_DK, tdQ = tmem + C::TM_DQ;
+      auto sq = [&](uint32_t g) { return sQD + (g % C::QSTAGE) * C::STAGE_BYTES; };
+      auto wait = [&](int b, uint32_t parity) {
+        return mbar_wait_bounded(bar(b), parity, tmo, f.err, abort_flag);
+      };
+      auto qd_ready = [&](uint32_t g) { return wait(FB_QD_FULL + g % C::QSTAGE, (g / C::QSTAGE) & 1); };
       uint32_t unit_cnt = 0, gs = 0;
       bool ok = true;
       int uslot = 0;
       uint32_t uph = 0;
       for (;; ++unit_cnt) {
-        if (!mbar_wait_bounded(bar(KB_U_FULL + uslot), uph, tmo, f.err, abort_flag)) { ok = false; break; }
+        if (!wait(FB_U_FULL + uslot, uph)) { ok = false; break; }
         const int u = uring[uslot];
-        mbar_arrive(bar(KB_U_EMPTY + uslot));
+        mbar_arrive(bar(FB_U_EMPTY + uslot));
         if (++uslot == 2) { uslot = 0; uph ^= 1; }
         if (u < 0) break;
         const KVUnit w = kv_unit(f, u);
-        if (!mbar_wait_bounded(bar(KB_KV_FULL), unit_cnt & 1, tmo, f.err, abort_flag)) { ok = false; break; }
+        if (!wait(FB_KV_FULL, unit_cnt & 1)) { ok = false; break; }
         tc_fence_after();
-        if (w.n_steps > 0) {
-          if (!mbar_wait_bounded(bar(KB_QD_FULL + gs % C::QSTAGE), (gs / C::QSTAGE) & 1, tmo, f.err,
-                                 abort_flag)) { ok = false; break; }
+        const uint32_t g0 = gs;
+        const int ns = w.n_steps;
+        if (ns > 0) {
+          if (!qd_ready(g0)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sq = sQD + (gs % C::QSTAGE) * C::STAGE_BYTES;
-          mma_s<D>(tS, sK, sq);              // S^T = K Q^T
-          tc_commit(bar(KB_S_FULL));
-          mma_s<D>(tdP, sV, sq + C::TILE);   // dP^T = V dO^T
-          tc_commit(bar(KB_DP_FULL));
+          mma_s<D>(tS, sK, sq(g0));  // S^T = K Q^T
+          tc_commit(bar(FB_S_FULL));
+          // dP^T lands where the previous step's dQ tile was (d = 128).
+          if (g0 > 0 && !wait(FB_DQ_READ, (g0 - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          mma_s<D>(tdP, sV, sq(g0) + C::TILE);  // dP^T = V dO^T
+          tc_commit(bar(FB_DP_FULL));
         }
         // The previous unit's accumulators must have been read out.
-        if (unit_cnt > 0 &&
-            !mbar_wait_bounded(bar(KB_ACC_EMPTY), (unit_cnt - 1) & 1, tmo, f.err, abort_flag)) { ok = false; break; }
-        for (int n = 0; n < w.n_steps; ++n) {
-          const uint32_t g = gs + n;
-          const uint32_t ph = g & 1;
-          const bool more = n + 1 < w.n_steps;
-          const uint32_t sq = sQD + (g % C::QSTAGE) * C::STAGE_BYTES;
-          const uint32_t sq1 = sQD + ((g + 1) % C::QSTAGE) * C::STAGE_BYTES;
-          if (!mbar_wait_bounded(bar(KB_P_FULL), ph, tmo, f.err, abort_flag)) { ok = false; break; }
+        if (unit_cnt > 0 && !wait(FB_ACC_EMPTY, (unit_cnt - 1) & 1)) { ok = false; break; }
+        if (ns > 0) {
+          if (!wait(FB_P_FULL, g0 & 1)) { ok = false; break; }
           tc_fence_after();
-          mma_acc<D>(tdV, tS, sq + C::TILE, n > 0);  // dV += P^T dO
-          if (more) {
-            // S(g+1) overwrites P^T(g): dV(g) is issued before it, and both
-            // warpgroups have read S(g) (they keep P in registers).
-            if (!mbar_wait_bounded(bar(KB_QD_FULL + (g + 1) % C::QSTAGE), ((g + 1) / C::QSTAGE) & 1, tmo,
-                                   f.err, abort_flag)) { ok = false; break; }
+          mma_acc<D>(tdV, tS, sq(g0) + C::TILE, 0);  // dV = P^T dO
+          if (ns > 1) {
+            if (!qd_ready(g0 + 1)) { ok = false; break; }
             tc_fence_after();
-            mma_s<D>(tS, sK, sq1);
-            tc_commit(bar(KB_S_FULL));
+            mma_s<D>(tS, sK, sq(g0 + 1));  // overwrites P^T(g0) after dV(g0) read it
+            tc_commit(bar(FB_S_FULL));
           }
-          if (!mbar_wait_bounded(bar(KB_DS_FULL), ph, tmo, f.err, abort_flag)) { ok = false; break; }
+        }
+        for (int n = 0; n < ns; ++n) {
+          const uint32_t g = g0 + n;
+          if (!wait(FB_DS_FULL, g & 1)) { ok = false; break; }
           tc_fence_after();
-          mma_acc<D>(tdK, tdP, sq, n > 0);  // dK += dS^T Q
-          tc_commit(bar(KB_QD_EMPTY + g % C::QSTAGE));
-          if (more) {
-            mma_s<D>(tdP, sV, sq1 + C::TILE);
-            tc_commit(bar(KB_DP_FULL));
+          mma_acc<D>(tdK, tdP, sq(g), n > 0);  // dK += dS^T Q
+          tc_commit(bar(FB_QD_EMPTY + g % C::QSTAGE));
+          mma_dq<D>(tdQ, sDS, sK);  // dQ tile = dS K
+          tc_commit(bar(FB_DQ_FULL));
+          if (n + 1 < ns) {
+            if (!wait(FB_P_FULL, (g + 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            mma_acc<D>(tdV, tS, sq(g + 1) + C::TILE, 1);  // dV += P^T dO
+            if (!wait(FB_DQ_READ, g & 1)) { ok = false; break; }
+            tc_fence_after();
+            mma_s<D>(tdP, sV, sq(g + 1) + C::TILE);
+            tc_commit(bar(FB_DP_FULL));
+            if (n + 2 < ns) {
+              if (!qd_ready(g + 2)) { ok = false; break; }
+              tc_fence_after();
+              mma_s<D>(tS, sK, sq(g + 2));
+              tc_commit(bar(FB_S_FULL));
+            }
           }
         }
         if (!ok) break;
-        gs += w.n_steps;
-        tc_commit(bar(KB_KV_EMPTY));
-        tc_commit(bar(KB_ACC_FULL));
+        gs += ns;
+        tc_commit(bar(FB_KV_EMPTY));
+        tc_commit(bar(FB_ACC_FULL));
       }
       volatile int no_abort = 0;
-      tc_commit(bar(KB_DRAIN));
-      mbar_wait_bounded(bar(KB_DRAIN), 0, 50000000ull, f.err, &no_abort);
+      tc_commit(bar(FB_DRAIN));
+      mbar_wait_bounded(bar(FB_DRAIN), 0, 50000000ull, f.err, &no_abort);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
+    using B = BCfg<D>;
     const int wg = (warp - 4) >> 2;  // warpgroup: columns [64 wg, 64 wg + 64) of every step
     const int c0 = 64 * wg;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::TM_S, tdP = tmem + lane_off + C::TM_DP;
+    const uint32_t tdQ = tmem + lane_off + C::TM_DQ + C::DQ_COLS * wg;
     const uint32_t tAcc = tmem + lane_off + (wg == 0 ? C::TM_DV : C::TM_DK);
     uint16_t* const out = static_cast<uint16_t*>(wg == 0 ? a.dv : a.dk);
+    // This thread's row (key r) of its warpgroup's 64-query sub-tile of dS.
+    const uint32_t ds_row = sDS + wg * B::SUB + r * 128;
+    const uint32_t r7 = static_cast<uint32_t>(r & 7);
     const float sl2 = f.scale_log2, scale = f.scale;
     uint32_t unit_cnt = 0, gs = 0;
     bool ok = true;
     int uslot = 0;
     uint32_t uph = 0;
     for (;; ++unit_cnt) {
-      const bool eu = mbar_wait_bounded(bar(KB_U_FULL + uslot), uph, tmo, f.err, abort_flag);
+      const bool eu = mbar_wait_bounded(bar(FB_U_FULL + uslot), uph, tmo, f.err, abort_flag);
       if (!__all_sync(0xffffffffu, eu)) { ok = false; break; }
       const int u = uring[uslot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(KB_U_EMPTY + uslot));
+      if (lane == 0) mbar_arrive(bar(FB_U_EMPTY + uslot));
       if (++uslot == 2) { uslot = 0; uph ^= 1; }
       if (u < 0) break;
       const KVUnit w = kv_unit(f, u);
@@ -555,15 +670,71 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         lo = f.causal ? j : __ldg(f.cu + dj);
         hi = min(__ldg(f.cu + dj + 1), w.qb);
       }
+      // dQ tile of a step out of tensor memory. d = 128: this thread holds
+      // dimension r of the warpgroup's 64 queries, and each warp-wide
+      // reduction covers 32 consecutive floats of one query's accumulator row
+      // (one 128-byte line). The 64 values are read at once (so that dP of the
+      // next step can reuse the columns) and kept as pending reductions that
+      // are issued in four groups of 16 spread over the next step's phases:
+      // the L2 takes reductions at a bounded rate, and issued in one burst
+      // they would hold up the warp.
+      // d = 64: this thread holds 32 dimensions of query row r, reduced at once.
+      uint32_t pend[64];
+      float* pend_p = nullptr;
+      int pend_nv = 0;  // columns whose query row exists (rows past the tile's last document receive nothing)
+      const size_t rs = static_cast<size_t>(f.Hq) * D;
+      auto flush = [&](auto lo_c, auto hi_c) {
+        constexpr int LO = decltype(lo_c)::value, HI = decltype(hi_c)::value;
+        if (pend_nv >= HI) {
+#pragma unroll
+          for (int c = LO; c < HI; ++c) red_add(pend_p + c * rs, pend[c]);
+        } else {
+#pragma unroll
+          for (int c = LO; c < HI; ++c)
+            if (c < pend_nv) red_add(pend_p + c * rs, pend[c]);
+        }
+      };
+      using I0 = std::integral_constant<int, 0>;
+      using I32 = std::integral_constant<int, 32>;
+      using I48 = std::integral_constant<int, 48>;
+      using I64 = std::integral_constant<int, 64>;
+      auto dq_take = [&](uint32_t g, int n) -> bool {
+        const bool e = mbar_wait_bounded(bar(FB_DQ_FULL), g & 1, tmo, f.err, abort_flag);
+        if (!__all_sync(0xffffffffu, e)) return false;
+        tc_fence_after();
+        const int h = w.hk * G + n % G;
+        if constexpr (D == 128) {
+          const int tq = w.qa + 128 * (n / G) + 64 * wg;  // query of this warpgroup's first column
+          tmem_ld64(tdQ, pend);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(FB_DQ_READ));
+          pend_p = a.dqacc + (static_cast<size_t>(tq) * f.Hq + h) * D + r;
+          pend_nv = w.qb - tq;
+        } else {
+          const int t = w.qa + 128 * (n / G) + r;
+          float* dst = a.dqacc + (static_cast<size_t>(t) * f.Hq + h) * D + 32 * wg;
+          uint32_t x[32];
+          tmem_ld32_sync(tdQ, x);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(FB_DQ_READ));
+          if (t < w.qb) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) red_add_v4(dst + i, x[i], x[i + 1], x[i + 2], x[i + 3]);
+          }
+        }
+        return true;
+      };
       for (int n = 0; n < w.n_steps; ++n) {
         const uint32_t g = gs + n;
         const uint32_t ph = g & 1;
         const int q0 = w.qa + 128 * (n / G);
         const uint8_t* stage = smem + C::OFF_QD + (g % C::QSTAGE) * C::STAGE_BYTES + 2 * C::TILE;
-        const uint32_t qd_bar = bar(KB_QD_FULL + g % C::QSTAGE), qd_ph = (g / C::QSTAGE) & 1;
-        // Both warpgroups: P for query columns [c0, c0 + 64), packed into
-        // S columns c0 .. c0+31; then dS for the same columns into dP.
-        bool e = mbar_wait_bounded(bar(KB_S_FULL), ph, tmo, f.err, abort_flag);
+        const uint32_t qd_bar = bar(FB_QD_FULL + g % C::QSTAGE), qd_ph = (g / C::QSTAGE) & 1;
+        if (D == 128 && n > 1) flush(I48{}, I64{});  // last group of step n-2's dQ tile
+        // P for query columns [c0, c0 + 64), packed into S columns c0 .. c0+31.
+        bool e = mbar_wait_bounded(bar(FB_S_FULL), ph, tmo, f.err, abort_flag);
         e = e && mbar_wait_bounded(qd_bar, qd_ph, tmo, f.err, abort_flag);
         if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
         tc_fence_after();
@@ -576,19 +747,38 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KB_P_FULL));
-        e = mbar_wait_bounded(bar(KB_DP_FULL), ph, tmo, f.err, abort_flag);
+        if (lane == 0) mbar_arrive(bar(FB_P_FULL));
+        // The previous step's dQ tile, while dV(g) runs.
+        if (n > 0) {
+          if (!dq_take(g - 1, n - 1)) { ok = false; break; }
+          if (D == 128) flush(I0{}, I32{});
+        }
+        // dS for the same columns: into dP (tensor memory) and dS (shared).
+        e = mbar_wait_bounded(bar(FB_DP_FULL), ph, tmo, f.err, abort_flag);
         if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
         tc_fence_after();
-        ds_half(tdP + c0, c0, p, scale, ColVals{reinterpret_cast<const float*>(stage + 512)});
+        ds_half(tdP + c0, c0, p, scale, ColVals{reinterpret_cast<const float*>(stage + 512)}, ds_row, r7,
+                [&] {
+                  if (D == 128 && n > 0) flush(I32{}, I48{});
+                });
         tmem_wait_st();
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KB_DS_FULL));
+        if (lane == 0) mbar_arrive(bar(FB_DS_FULL));
       }
       if (!ok) break;
+      if (D == 128 && w.n_steps > 1) flush(I48{}, I64{});
+      if (w.n_steps > 0) {
+        if (!dq_take(gs + w.n_steps - 1, w.n_steps - 1)) { ok = false; break; }
+        if (D == 128) {
+          flush(I0{}, I32{});
+          flush(I32{}, I48{});
+          flush(I48{}, I64{});
+        }
+      }
       gs += w.n_steps;
-      const bool e = mbar_wait_bounded(bar(KB_ACC_FULL), unit_cnt & 1, tmo, f.err, abort_flag);
+      const bool e = mbar_wait_bounded(bar(FB_ACC_FULL), unit_cnt & 1, tmo, f.err, abort_flag);
       if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
       tc_fence_after();
       // Warpgroup 0 writes dV, warpgroup 1 dK.
@@ -605,385 +795,7 @@ bwd_dkdv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(KB_ACC_EMPTY));
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
-
-// ------------------------------------------------------------------ dQ
-
-template <int D>
-struct QCfg : BCfg<D> {
-  using B = BCfg<D>;
-  // K tile g is read by S(g) and dQ(g), the last MMA of step g; V tile g only
-  // by dP(g), issued a step earlier. So K has one stage more than V: the copy
-  // of step g+3's K starts when dQ(g) is done and has a whole step to land.
-  static constexpr int KSTAGE = 3;
-  static constexpr int VSTAGE = 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = B::TILE;
-  static constexpr int OFF_K = 2 * B::TILE;
-  static constexpr int OFF_V = OFF_K + KSTAGE * B::TILE;
-  static constexpr int OFF_BAR = OFF_V + VSTAGE * B::TILE;
-  static constexpr int N_BARS = 24;
-  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
-  static constexpr int OFF_UREC = OFF_MISC + 16;  // two unit records
-  static constexpr int SMEM_ALLOC = OFF_UREC + 2 * 64 + 1024;
-  static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;
-};
-
-// KV_FULL[s] completes when K stage s and the V tile loaded with it have landed.
-enum { QB_Q_FULL = 0, QB_Q_EMPTY = 1, QB_KV_FULL = 2, QB_K_EMPTY = 5, QB_V_EMPTY = 8, QB_S_FULL = 10,
-       QB_DP_FULL = 11, QB_S_READ = 12, QB_DS_FULL = 13, QB_ACC_FULL = 14, QB_ACC_EMPTY = 15,
-       QB_DRAIN = 16, QB_U_FULL = 17, QB_U_EMPTY = 19 };
-
-// dQ unit record (int32 words; slot stride 16 words): what every role needs to
-// run a unit, built once by the scheduler warp: the unit (< 0: no more work),
-// its query head and first row, its Q tile (bounds and documents), the cursor
-// standing on its first key tile, and the number of key tiles.
-enum { DR_V = 0, DR_H = 1, DR_Q0 = 2, DR_QT = 3, DR_CUR = 8, DR_NBLK = 14, DR_N = 15 };
-constexpr int DQ_UNIT_CONSUMERS = 10;  // producer, MMA lane, eight compute warps
-
-template <int D>
-__global__ void __launch_bounds__(384, 1)
-bwd_dq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
-              const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-              const __grid_constant__ CUtensorMap tmdo) {
-  using C = QCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO;
-  auto sk = [&](uint32_t g) { return sbase + C::OFF_K + (g % C::KSTAGE) * C::TILE; };
-  auto sv = [&](uint32_t g) { return sbase + C::OFF_V + (g % C::VSTAGE) * C::TILE; };
-  const uint32_t bar0 = sbase + C::OFF_BAR;
-  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  volatile int* urec = reinterpret_cast<volatile int*>(smem + C::OFF_UREC);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar(QB_Q_FULL), 1);
-    mbar_init(bar(QB_Q_EMPTY), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(QB_U_FULL + s), 1);
-      mbar_init(bar(QB_U_EMPTY + s), DQ_UNIT_CONSUMERS);
-    }
-    for (int s = 0; s < C::KSTAGE; ++s) {
-      mbar_init(bar(QB_KV_FULL + s), 1);
-      mbar_init(bar(QB_K_EMPTY + s), 1);
-    }
-    for (int s = 0; s < C::VSTAGE; ++s) mbar_init(bar(QB_V_EMPTY + s), 1);
-    mbar_init(bar(QB_S_FULL), 1);
-    mbar_init(bar(QB_DP_FULL), 1);
-    mbar_init(bar(QB_S_READ), 8);   // both compute warpgroups, one arrival per warp
-    mbar_init(bar(QB_DS_FULL), 8);
-    mbar_init(bar(QB_ACC_FULL), 1);
-    mbar_init(bar(QB_ACC_EMPTY), 8);
-    mbar_init(bar(QB_DRAIN), 1);
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const AttnArgs& f = a.fwd;
-  const int n_units = n_units_of(f);
-  const int G = f.Hq / f.Hkv;
-  const unsigned long long tmo = f.timeout_ns;
-
-  // Units reach every role as records in a two-slot ring (see DR_*). Reads
-  // one (the caller arrives on its slot's EMPTY barrier afterwards): false on
-  // a timeout. The unit's single Q tile is qt[0]; qt[1] stays empty.
-  auto read_unit = [&](int slot, uint32_t ph, int& v, int& h, int& q0, QTile (&qt)[2], Cursor& cur,
-                       int& nblk) -> bool {
-    if (!mbar_wait_bounded(bar(QB_U_FULL + slot), ph, tmo, f.err, abort_flag)) return false;
-    const volatile int* rs = urec + 16 * slot;
-    v = rs[DR_V];
-    if (v < 0) return true;
-    h = rs[DR_H];
-    q0 = rs[DR_Q0];
-    qt[0].qa = rs[DR_QT + 0];
-    qt[0].qb = rs[DR_QT + 1];
-    qt[0].ds = rs[DR_QT + 2];
-    qt[0].de = rs[DR_QT + 3];
-    qt[0].one_doc = rs[DR_QT + 4];
-    qt[1].qa = qt[1].qb = qt[1].ds = qt[1].de = qt[1].one_doc = 0;
-    cur.item = rs[DR_CUR + 0];
-    cur.item_end = rs[DR_CUR + 1];
-    cur.kv_e = rs[DR_CUR + 2];
-    cur.k0 = rs[DR_CUR + 3];
-    cur.lo = rs[DR_CUR + 4];
-    cur.hi = rs[DR_CUR + 5];
-    nblk = rs[DR_NBLK];
-    return true;
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t kv_cnt = 0, unit_cnt = 0;
-      int armed_q = 0, armed_kv[C::KSTAGE] = {};
-      uint32_t par_q = 0, par_kv[C::KSTAGE] = {};
-      bool ok = true;
-      for (;; ++unit_cnt) {
-        int v = -1, h = 0, q0 = 0, nblk = 0;
-        QTile qt[2];
-        Cursor cur;
-        if (!read_unit(unit_cnt & 1, (unit_cnt >> 1) & 1, v, h, q0, qt, cur, nblk)) { ok = false; break; }
-        mbar_arrive(bar(QB_U_EMPTY + (unit_cnt & 1)));
-        if (v < 0) break;
-        const int hk = h / G;
-        if (!mbar_wait_bounded(bar(QB_Q_EMPTY), (unit_cnt & 1) ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(QB_Q_FULL), 2 * C::TILE);
-        armed_q = 1;
-        par_q = unit_cnt & 1;
-        load_rows128<D>(sQ, &tmq, bar(QB_Q_FULL), h, q0, f.T);
-        load_rows128<D>(sDO, &tmdo, bar(QB_Q_FULL), h, q0, f.T);
-        int ka, kb, cls[2];
-        while (next_tile(f, cur, qt, ka, kb, cls)) {
-          const int st = kv_cnt % C::KSTAGE, vs = kv_cnt % C::VSTAGE;
-          const uint32_t ph = (kv_cnt / C::KSTAGE) & 1, vph = (kv_cnt / C::VSTAGE) & 1;
-          if (!mbar_wait_bounded(bar(QB_K_EMPTY + st), ph ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
-          if (!mbar_wait_bounded(bar(QB_V_EMPTY + vs), vph ^ 1, tmo, f.err, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(QB_KV_FULL + st), 2 * C::TILE);
-          armed_kv[st] = 1;
-          par_kv[st] = ph;
-          load_rows128<D>(sk(kv_cnt), &tmk, bar(QB_KV_FULL + st), hk, ka, f.T);
-          load_rows128<D>(sv(kv_cnt), &tmv, bar(QB_KV_FULL + st), hk, ka, f.T);
-          ++kv_cnt;
-        }
-        if (!ok) break;
-      }
-      if (!ok) {
-        volatile int no_abort = 0;
-        if (armed_q) mbar_wait_bounded(bar(QB_Q_FULL), par_q, 50000000ull, f.err, &no_abort);
-        for (int s = 0; s < C::KSTAGE; ++s)
-          if (armed_kv[s]) mbar_wait_bounded(bar(QB_KV_FULL + s), par_kv[s], 50000000ull, f.err, &no_abort);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA lane
-    if (lane == 0) {
-      const uint32_t tS = tmem + C::TM_S, tdP = tmem + C::TM_DP, tdQ = tmem + C::TM_DQ;
-      uint32_t kv_cnt = 0, unit_cnt = 0;
-      bool ok = true;
-      for (;; ++unit_cnt) {
-        int v = -1, h = 0, q0 = 0, nblk = 0;
-        QTile qt[2];
-        Cursor cur;
-        if (!read_unit(unit_cnt & 1, (unit_cnt >> 1) & 1, v, h, q0, qt, cur, nblk)) { ok = false; break; }
-        mbar_arrive(bar(QB_U_EMPTY + (unit_cnt & 1)));
-        if (v < 0) break;
-        if (!mbar_wait_bounded(bar(QB_Q_FULL), unit_cnt & 1, tmo, f.err, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        if (nblk > 0) {
-          const uint32_t g = kv_cnt;
-          if (!mbar_wait_bounded(bar(QB_KV_FULL + g % C::KSTAGE), (g / C::KSTAGE) & 1, tmo, f.err,
-                                 abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          mma_s<D>(tS, sQ, sk(g));          // S = Q K^T
-          tc_commit(bar(QB_S_FULL));
-          mma_s<D>(tdP, sDO, sv(g));        // dP = dO V^T
-          tc_commit(bar(QB_DP_FULL));
-          tc_commit(bar(QB_V_EMPTY + g % C::VSTAGE));
-        }
-        if (unit_cnt > 0 &&
-            !mbar_wait_bounded(bar(QB_ACC_EMPTY), (unit_cnt - 1) & 1, tmo, f.err, abort_flag)) { ok = false; break; }
-        for (int n = 0; n < nblk; ++n) {
-          const uint32_t g = kv_cnt + n;
-          const uint32_t ph = g & 1;
-          const bool more = n + 1 < nblk;
-          if (more) {
-            // Both warpgroups have read S(g): S may be overwritten.
-            if (!mbar_wait_bounded(bar(QB_S_READ), ph, tmo, f.err, abort_flag)) { ok = false; break; }
-            if (!mbar_wait_bounded(bar(QB_KV_FULL + (g + 1) % C::KSTAGE), ((g + 1) / C::KSTAGE) & 1, tmo,
-                                   f.err, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            mma_s<D>(tS, sQ, sk(g + 1));
-            tc_commit(bar(QB_S_FULL));
-          }
-          if (!mbar_wait_bounded(bar(QB_DS_FULL), ph, tmo, f.err, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          mma_acc<D>(tdQ, tdP, sk(g), n > 0);  // dQ += dS K
-          tc_commit(bar(QB_K_EMPTY + g % C::KSTAGE));
-          if (more) {
-            mma_s<D>(tdP, sDO, sv(g + 1));
-            tc_commit(bar(QB_DP_FULL));
-            tc_commit(bar(QB_V_EMPTY + (g + 1) % C::VSTAGE));
-          }
-        }
-        if (!ok) break;
-        kv_cnt += nblk;
-        tc_commit(bar(QB_Q_EMPTY));
-        tc_commit(bar(QB_ACC_FULL));
-      }
-      volatile int no_abort = 0;
-      tc_commit(bar(QB_DRAIN));
-      mbar_wait_bounded(bar(QB_DRAIN), 0, 50000000ull, f.err, &no_abort);
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ unit scheduler
-    // Claims units (from the set-up kernel's queue, largest groups first, or
-    // strided over the CTAs) and builds each one's record ahead of the other
-    // roles: the table searches and the walk over the unit's items (to count
-    // its key tiles and find the first) are off their path.
-    if (lane == 0) {
-      int k_static = 0;
-      for (uint32_t cnt = 0;; ++cnt) {
-        int v;
-        if (f.work_counter) {
-          v = atomicAdd(f.work_counter, 1);
-        } else {
-          v = static_cast<int>(blockIdx.x) + k_static * static_cast<int>(gridDim.x);
-          ++k_static;
-        }
-        if (v >= n_units) v = -1;
-        int w[DR_N];
-        w[DR_V] = v;
-        if (v >= 0) {
-          const UnitInfo ui = unit_info(f, v);
-          QTile qt[2];
-          qt[0] = make_qtile(f, ui, 0);
-          qt[1].qa = qt[1].qb = qt[1].ds = qt[1].de = qt[1].one_doc = 0;
-          Cursor cur = make_cursor(f, ui, qt, f.causal);
-          Cursor walk = cur;
-          int ka, kb, cls[2], nblk = 0;
-          while (next_tile(f, walk, qt, ka, kb, cls)) {
-            if (nblk == 0) {
-              cur = walk;
-              cur.k0 = ka;  // standing on the first tile
-            }
-            ++nblk;
-          }
-          w[DR_H] = ui.h;
-          w[DR_Q0] = ui.q0;
-          w[DR_QT + 0] = qt[0].qa;
-          w[DR_QT + 1] = qt[0].qb;
-          w[DR_QT + 2] = qt[0].ds;
-          w[DR_QT + 3] = qt[0].de;
-          w[DR_QT + 4] = qt[0].one_doc;
-          w[DR_CUR + 0] = cur.item;
-          w[DR_CUR + 1] = cur.item_end;
-          w[DR_CUR + 2] = cur.kv_e;
-          w[DR_CUR + 3] = cur.k0;
-          w[DR_CUR + 4] = cur.lo;
-          w[DR_CUR + 5] = cur.hi;
-          w[DR_NBLK] = nblk;
-        }
-        const int slot = cnt & 1;
-        if (!mbar_wait_bounded(bar(QB_U_EMPTY + slot), ((cnt >> 1) & 1) ^ 1, tmo, f.err, abort_flag)) break;
-        volatile int* rs = urec + 16 * slot;
-        const int n = v >= 0 ? static_cast<int>(DR_N) : 1;
-        for (int i = 0; i < n; ++i) rs[i] = w[i];
-        mbar_arrive(bar(QB_U_FULL + slot));
-        if (v < 0) break;
-      }
-    }
-    __syncwarp();
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ compute
-    const int wg = (warp - 4) >> 2;  // warpgroup: columns [64 wg, 64 wg + 64) of every block
-    const int c0 = 64 * wg;
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::TM_S, tdP = tmem + lane_off + C::TM_DP;
-    const uint32_t tdQ = tmem + lane_off + C::TM_DQ;
-    const float sl2 = f.scale_log2, scale = f.scale;
-    uint32_t unit_cnt = 0, g = 0;
-    bool ok = true;
-    for (;; ++unit_cnt) {
-      int v = -1, h = 0, q0 = 0, nblk_u = 0;
-      QTile qt[2];
-      Cursor cur;
-      const bool got = read_unit(unit_cnt & 1, (unit_cnt >> 1) & 1, v, h, q0, qt, cur, nblk_u);
-      __syncwarp();
-      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-      if (lane == 0) mbar_arrive(bar(QB_U_EMPTY + (unit_cnt & 1)));
-      if (v < 0) break;
-      const int t = q0 + r;
-      const bool valid = t >= qt[0].qa && t < qt[0].qb;
-      int rds = 0, rde = 0;
-      float nlse2 = 0.f, ndsc = 0.f;
-      if (valid) {
-        if (qt[0].one_doc) {  // the tile's rows are all in one document
-          rds = qt[0].ds;
-          rde = qt[0].de;
-        } else {
-          const int dd = doc_of(f.cu, f.ndocs, t);
-          rds = __ldg(f.cu + dd);
-          rde = __ldg(f.cu + dd + 1);
-        }
-        nlse2 = __ldg(a.nlse2 + static_cast<size_t>(h) * f.T + t);
-        ndsc = __ldg(a.ndsc + static_cast<size_t>(h) * f.T + t);
-      }
-      const int rend = f.causal ? min(rde, t + 1) : rde;
-      int nblk = 0;
-      int ka, kb, cls[2];
-      while (next_tile(f, cur, qt, ka, kb, cls)) {
-        const uint32_t ph = g & 1;
-        // Both warpgroups: P for key columns [c0, c0 + 64) in registers, then
-        // dS for the same columns into dP.
-        bool e = mbar_wait_bounded(bar(QB_S_FULL), ph, tmo, f.err, abort_flag);
-        if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t p[64];
-        tmem_ld64(tS + c0, p);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(QB_S_READ));
-        int lo = 0, hi = 128;
-        if (cls[0] != CLS_FULL) {
-          lo = valid ? max(ka, rds) - ka : 0;
-          hi = valid ? min(kb, rend) - ka : 0;
-        }
-        p_half(c0, lo, hi, sl2, RowVal{f2_pack(nlse2, nlse2)}, p);
-        e = mbar_wait_bounded(bar(QB_DP_FULL), ph, tmo, f.err, abort_flag);
-        if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-        tc_fence_after();
-        ds_half(tdP + c0, c0, p, scale, RowVal{f2_pack(ndsc, ndsc)});
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(QB_DS_FULL));
-        ++g;
-        ++nblk;
-      }
-      if (!ok) break;
-      const bool e = mbar_wait_bounded(bar(QB_ACC_FULL), unit_cnt & 1, tmo, f.err, abort_flag);
-      if (!__all_sync(0xffffffffu, e)) { ok = false; break; }
-      tc_fence_after();
-      // Each warpgroup writes half of the dQ columns.
-#pragma unroll 1
-      for (int ch = wg * (D / 64); ch < (wg + 1) * (D / 64); ++ch) {
-        uint32_t rq[32];
-        if (nblk > 0) tmem_ld32_sync(tdQ + 32 * ch, rq);
-        if (valid) {
-          uint16_t* dst = static_cast<uint16_t*>(a.dq) + (static_cast<size_t>(t) * f.Hq + h) * D + 32 * ch;
-          if (nblk > 0) store_row32_bf16(dst, rq);
-          else store_zero_row_bf16(dst, 32);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(QB_ACC_EMPTY));
+      if (lane == 0) mbar_arrive(bar(FB_ACC_EMPTY));
     }
   }
   tc_fence_before();
@@ -1006,9 +818,10 @@ cudaError_t launch_cfg(K kern, int grid, cudaStream_t st, const BwdArgs& a, cons
 }  // namespace
 
 cudaError_t launch_bwd_rowdot(const void* o, const void* dout, const float* lse, float* ndsc, float* nlse2,
-                              int T, int Hq, int d, float scale, int grid, cudaStream_t st) {
+                              float* dqacc, int32_t* unit_counter, int T, int Hq, int d, float scale, int grid,
+                              cudaStream_t st) {
   bwd_rowdot_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                         lse, ndsc, nlse2, T, Hq, d, scale);
+                                         lse, ndsc, nlse2, dqacc, unit_counter, T, Hq, d, scale);
   return cudaGetLastError();
 }
 
@@ -1021,15 +834,15 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, const void* tq, const void* tk, cons
   memcpy(&mdo, tdo, sizeof mdo);
   const long long kv_units = static_cast<long long>((a.fwd.T + 127) / 128) * a.fwd.Hkv;
   const int kv_grid = static_cast<int>(kv_units < grid ? kv_units : grid);
-  cudaError_t e;
-  if (a.fwd.d == 128) {
-    e = launch_cfg<QCfg<128>>(bwd_dq_kernel<128>, grid, st, a, mq, mk, mv, mdo);
-    if (e != cudaSuccess) return e;
-    return launch_cfg<KVCfg<128>>(bwd_dkdv_kernel<128>, kv_grid, st, a, mq, mk, mv, mdo);
-  }
-  e = launch_cfg<QCfg<64>>(bwd_dq_kernel<64>, grid, st, a, mq, mk, mv, mdo);
+  cudaError_t e = a.fwd.d == 128
+                      ? launch_cfg<FCfg<128>>(bwd_fused_kernel<128>, kv_grid, st, a, mq, mk, mv, mdo)
+                      : launch_cfg<FCfg<64>>(bwd_fused_kernel<64>, kv_grid, st, a, mq, mk, mv, mdo);
   if (e != cudaSuccess) return e;
-  return launch_cfg<KVCfg<64>>(bwd_dkdv_kernel<64>, kv_grid, st, a, mq, mk, mv, mdo);
+  const long long n8 = static_cast<long long>(a.fwd.T) * a.fwd.Hq * a.fwd.d / 8;
+  long long cgrid = (n8 + 255) / 256;
+  if (cgrid > static_cast<long long>(grid) * 8) cgrid = static_cast<long long>(grid) * 8;
+  bwd_dq_convert_kernel<<<static_cast<int>(cgrid), 256, 0, st>>>(a.dqacc, static_cast<uint16_t*>(a.dq), n8);
+  return cudaGetLastError();
 }
 
 }  // namespace sp

@@ -253,13 +253,37 @@ sp_status sp_packed_attention_ex(const void* q, const void* k, const void* v, vo
   return launch_attention(a, dtype, sms, st, 0, item_heads_dev == nullptr);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Backward workspace: [header (the unit counter)][-scale D][-LSE log2 e]
+// [fp32 dQ accumulator]; each part 256-byte aligned. The accumulator is sized
+// for d = 128, the largest head dimension.
+struct BwdWs {
+  size_t off_ndsc, off_nlse2, off_dqacc, total;
+};
+
+BwdWs bwd_ws(int32_t T, int32_t Hq) {
+  auto r256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t rows = static_cast<size_t>(T) * static_cast<size_t>(Hq);
+  BwdWs L;
+  L.off_ndsc = r256(sp::WS_HEADER_WORDS * sizeof(int32_t));
+  L.off_nlse2 = L.off_ndsc + r256(rows * sizeof(float));
+  L.off_dqacc = L.off_nlse2 + r256(rows * sizeof(float));
+  L.total = L.off_dqacc + r256(rows * 128 * sizeof(float));
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t sp_packed_attention_backward_workspace_size(int64_t n_items, int32_t T, int32_t Hq) {
-  if (n_items < 0) n_items = 0;
+  (void)n_items;
   if (T < 0) T = 0;
   if (Hq < 0) Hq = 0;
-  // D and LSE * log2(e) per (head, row).
-  const size_t rowdot = (static_cast<size_t>(T) * Hq * sizeof(float) + 255) & ~static_cast<size_t>(255);
-  return sp::ws_layout(n_items).total + 2 * rowdot;
+  return bwd_ws(T, Hq).total;
 }
 
 sp_status sp_packed_attention_backward(const void* q, const void* k, const void* v, const void* o,
@@ -289,35 +313,28 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   if (!device_state(&err, &sms)) return SP_ERR_CUDA;
   if (!encoder()) return SP_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const sp::WsLayout L = sp::ws_layout(n_items);
-  // After the set-up kernel's layout: -scale D and -LSE log2 e, [Hq][T] fp32 each.
-  float* ndsc = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.total);
-  float* nlse2 = reinterpret_cast<float*>(
-      static_cast<char*>(workspace) + L.total +
-      ((static_cast<size_t>(T) * Hq * sizeof(float) + 255) & ~static_cast<size_t>(255)));
+  const BwdWs L = bwd_ws(T, Hq);
+  char* ws = static_cast<char*>(workspace);
+  float* ndsc = reinterpret_cast<float*>(ws + L.off_ndsc);
+  float* nlse2 = reinterpret_cast<float*>(ws + L.off_nlse2);
+  float* dqacc = reinterpret_cast<float*>(ws + L.off_dqacc);
+  int32_t* unit_counter = reinterpret_cast<int32_t*>(ws) + sp::WS_BWD_COUNTER;
 
   const long long warps = static_cast<long long>(T) * Hq;
   long long g = (warps + 7) / 8;
   if (g > static_cast<long long>(sms) * 16) g = static_cast<long long>(sms) * 16;
-  cudaError_t e = sp::launch_bwd_rowdot(o, dout, lse, ndsc, nlse2, T, Hq, d, scale, static_cast<int>(g), st);
-  if (e != cudaSuccess) return SP_ERR_CUDA;
-  e = sp::launch_prep(items_dev, nullptr, n_items, T, Hq, Hkv, sp::BWD_ROWS_PER_UNIT, workspace, err, st);
+  cudaError_t e = sp::launch_bwd_rowdot(o, dout, lse, ndsc, nlse2, dqacc, unit_counter, T, Hq, d, scale,
+                                        static_cast<int>(g), st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
 
   sp::BwdArgs b;
   std::memset(&b, 0, sizeof b);
   b.fwd = base_args(q, k, v, nullptr, nullptr, T, Hq, Hkv, d, cu_seqlens_dev, ndocs, causal, scale, err);
-  b.fwd.items = items_dev;
-  b.fwd.item_order = reinterpret_cast<const int32_t*>(static_cast<const char*>(workspace) + L.off_order);
-  b.fwd.header = static_cast<const int32_t*>(workspace);
-  b.fwd.segs = reinterpret_cast<const sp::SegEntry*>(static_cast<const char*>(workspace) + L.off_segs);
-  b.fwd.rows_per_unit = sp::BWD_ROWS_PER_UNIT;
-  b.fwd.work_counter = static_cast<int32_t*>(workspace) + sp::WS_COUNTER;  // dQ units, reset by the set-up kernel
   b.lse = lse;
   b.ndsc = ndsc;
   b.nlse2 = nlse2;
-  b.unit_counter = static_cast<int32_t*>(workspace) + sp::WS_BWD_COUNTER;
-  if (cudaMemsetAsync(b.unit_counter, 0, sizeof(int32_t), st) != cudaSuccess) return SP_ERR_CUDA;
+  b.unit_counter = unit_counter;
+  b.dqacc = dqacc;
   b.dq = dq;
   b.dk = dk;
   b.dv = dv;

@@ -74,7 +74,8 @@ struct BwdArgs {
   const float* lse;    // [Hq][T] natural-log LSE written by the forward
   const float* ndsc;   // [Hq][T] -scale * D_i, D_i = dO_i . O_i
   const float* nlse2;  // [Hq][T] -LSE_i * log2(e)
-  int32_t* unit_counter;  // dK/dV work-unit queue (zeroed before the launch)
+  int32_t* unit_counter;  // fused kernel's work-unit queue (zeroed by the row-dot kernel)
+  float* dqacc;       // fp32 [T][Hq][d] dQ accumulator (zeroed by the row-dot kernel)
   void* dq;           // bf16 [T][Hq][d]
   void* dk;           // bf16 [T][Hkv][d]
   void* dv;           // bf16 [T][Hkv][d]
@@ -97,8 +98,10 @@ cudaError_t launch_attn_tc_pair(const AttnArgs& a, const void* tmap_q, const voi
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
                              int32_t rows, int32_t Hq, int32_t d, int grid, cudaStream_t st);
 cudaError_t launch_bwd_rowdot(const void* o, const void* dout, const float* lse, float* ndsc, float* nlse2,
-                              int T, int Hq, int d, float scale, int grid, cudaStream_t st);
-// dQ kernel (walks the schedule in fwd) then the dK/dV kernel, both bf16.
+                              float* dqacc, int32_t* unit_counter, int T, int Hq, int d, float scale, int grid,
+                              cudaStream_t st);
+// The fused dK/dV/dQ kernel (key/value tiles stationary, dQ reduced into
+// dqacc), then dQ rounded from dqacc to bf16.
 cudaError_t launch_bwd_tc(const BwdArgs& a, const void* tmap_q, const void* tmap_k,
                           const void* tmap_v, const void* tmap_do, int grid, cudaStream_t st);
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t st);
