@@ -224,7 +224,9 @@ sp_status sp_schedule_link_bytes_hier(sp_sched_kind inter_kind, int32_t R, int32
  *           CUDA cores in fp32 for the 1e-5 tolerance).
  *  o_part: device float32 [q_end - q_begin][Hq][d]; lse_part: device float32
  *          [Hq][q_end - q_begin].
- *  cu_seqlens_dev: device int32 [ndocs + 1] (validity is the caller's duty).
+ *  cu_seqlens_dev: device int32 [ndocs + 1]. Not checked here (no set-up
+ *           kernel runs): a malformed descriptor changes the masks but every
+ *           access stays within the Q rows and key range given.
  *  d must be 64 or 128. An empty row range is a no-op. */
 sp_status sp_partial_attn(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
                           int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,
@@ -266,7 +268,15 @@ size_t sp_packed_attention_workspace_size(int64_t n_items);
  *  merges its items' partials is free (the log-sum-exp merge is associative):
  *  items that are not whole 128-key tiles long are visited in key order, and
  *  contiguous key ranges are walked as one.
- *  An inconsistent item list is reported through sp_check_device_status. */
+ *  Checked on the device before anything is written (a failure is reported
+ *  as SP_ERR_INTERNAL through sp_check_device_status, and no output is
+ *  touched): cu_seqlens_dev is a packing descriptor of [0, T) (cu[0] = 0,
+ *  strictly increasing, cu[ndocs] = T); every item lies in [0, T) and holds
+ *  at least one (query, key) pair the masks allow under it, as a pruned
+ *  schedule built from the same descriptor does (an item without one means
+ *  the schedule was built for another packing); the items form at most 8192
+ *  groups (runs sharing a rank, Q range and head range) whose Q ranges do
+ *  not overlap. */
 sp_status sp_packed_attention(const void* q, const void* k, const void* v, void* o, float* lse,
                               int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,
                               const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal, float scale,
@@ -350,6 +360,8 @@ size_t sp_packed_attention_backward_workspace_size(int64_t n_items, int32_t T, i
  *  dtype must be SP_DTYPE_BF16 (SP_ERR_UNSUPPORTED otherwise); d is 64 or 128.
  *  workspace: device, at least sp_packed_attention_backward_workspace_size
  *     bytes, owned by the caller; calls sharing it must not overlap in time.
+ *  cu_seqlens_dev is checked on the device as in sp_packed_attention; a bad
+ *  one is reported as SP_ERR_INTERNAL and dq, dk, dv are not touched.
  *  Timeouts of the kernels' bounded waits are reported through
  *  sp_check_device_status. */
 sp_status sp_packed_attention_backward(const void* q, const void* k, const void* v, const void* o,

@@ -304,15 +304,33 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, int c0, const uint32_t (&
 // nlse2[h][t] = -lse[h][t] * log2(e); one warp per (t, h). The signs and the
 // scale are folded in so that the tensor-core kernel needs one FMA per value.
 // Also zeroes the (t, h) row of the fp32 dQ accumulator [T][Hq][d] and the
-// fused kernel's unit counter, which the next kernel on the stream reads.
+// fused kernel's unit counter, which the next kernel on the stream reads, and
+// (block 0) checks the packing descriptor the masks come from: cu[0] = 0,
+// strictly increasing, cu[ndocs] = T. A bad one sets *status, which makes the
+// next two kernels write nothing (their row ranges come from it), and records
+// ERR_INTERNAL.
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restrict__ o,
                                                          const uint16_t* __restrict__ dout,
                                                          const float* __restrict__ lse,
                                                          float* __restrict__ ndsc, float* __restrict__ nlse2,
                                                          float* __restrict__ dqacc, int32_t* unit_counter,
-                                                         int T, int Hq, int d, float scale) {
+                                                         int32_t* status, const int32_t* __restrict__ cu,
+                                                         int ndocs, unsigned* err, int T, int Hq, int d,
+                                                         float scale) {
   const int lane = threadIdx.x & 31;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *unit_counter = 0;
+  if (blockIdx.x == 0) {
+    int bad = 0;
+    for (int i = threadIdx.x; i <= ndocs; i += blockDim.x) {
+      const int c = __ldg(cu + i);
+      if ((i == 0 && c != 0) || (i == ndocs && c != T) || (i < ndocs && c >= __ldg(cu + i + 1))) bad = 1;
+    }
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+      *unit_counter = 0;
+      *status = bad;
+      if (bad) atomicOr(err, ERR_INTERNAL_BIT);
+    }
+  }
   const long long n = static_cast<long long>(T) * Hq;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -341,7 +359,9 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restr
 
 // dq = bf16(acc), 8 elements per thread and pass (n8 = elements / 8).
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ acc,
-                                                             uint16_t* __restrict__ dq, long long n8) {
+                                                             uint16_t* __restrict__ dq, long long n8,
+                                                             const int32_t* status) {
+  if (*status) return;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
     const float4 x = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
@@ -422,6 +442,7 @@ bwd_fused_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq,
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const AttnArgs& f = a.fwd;
+  if (*a.status) return;  // cu_seqlens failed the row-dot kernel's check: nothing is written
   if (sbase & 1023u) {  // the layout has no slack to realign (see FCfg)
     if (threadIdx.x == 0) atomicOr(f.err, ERR_INTERNAL_BIT);
     return;
@@ -818,10 +839,12 @@ cudaError_t launch_cfg(K kern, int grid, cudaStream_t st, const BwdArgs& a, cons
 }  // namespace
 
 cudaError_t launch_bwd_rowdot(const void* o, const void* dout, const float* lse, float* ndsc, float* nlse2,
-                              float* dqacc, int32_t* unit_counter, int T, int Hq, int d, float scale, int grid,
+                              float* dqacc, int32_t* unit_counter, int32_t* status, const int32_t* cu,
+                              int ndocs, unsigned* err, int T, int Hq, int d, float scale, int grid,
                               cudaStream_t st) {
   bwd_rowdot_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                         lse, ndsc, nlse2, dqacc, unit_counter, T, Hq, d, scale);
+                                         lse, ndsc, nlse2, dqacc, unit_counter, status, cu, ndocs, err, T, Hq,
+                                         d, scale);
   return cudaGetLastError();
 }
 
@@ -841,7 +864,8 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, const void* tq, const void* tk, cons
   const long long n8 = static_cast<long long>(a.fwd.T) * a.fwd.Hq * a.fwd.d / 8;
   long long cgrid = (n8 + 255) / 256;
   if (cgrid > static_cast<long long>(grid) * 8) cgrid = static_cast<long long>(grid) * 8;
-  bwd_dq_convert_kernel<<<static_cast<int>(cgrid), 256, 0, st>>>(a.dqacc, static_cast<uint16_t*>(a.dq), n8);
+  bwd_dq_convert_kernel<<<static_cast<int>(cgrid), 256, 0, st>>>(a.dqacc, static_cast<uint16_t*>(a.dq), n8,
+                                                                a.status);
   return cudaGetLastError();
 }
 

@@ -31,6 +31,8 @@
 
 #include <cuda.h>
 
+#include <mutex>
+
 #include "sp_device.cuh"
 #include "sp_tiles.cuh"
 
@@ -579,14 +581,21 @@ cudaError_t launch_one(const AttnArgs& a, const void* tq, const void* tk, const 
                        cudaStream_t st) {
   using C = Cfg<D>;
   auto kern = attn_tc_kernel<D, OUT_FP32>;
-  static int configured_mask = 0;  // per-device bit (devices < 32)
+  // The shared-memory attribute is a per-device setting: set once per device,
+  // under a lock shared by host threads.
+  static std::mutex mu;
+  static bool configured[MAX_DEVICES] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(configured_mask & (1 << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    configured_mask |= 1 << (dev & 31);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
   }
   CUtensorMap mq, mk, mv;
   memcpy(&mq, tq, sizeof mq);

@@ -33,6 +33,8 @@
 
 #include <cuda.h>
 
+#include <mutex>
+
 #include "sp_device.cuh"
 #include "sp_tiles.cuh"
 
@@ -794,10 +796,16 @@ cudaError_t launch_pair(const AttnArgs& a, const void* tq, const void* tk, const
                         cudaStream_t st) {
   using C = PCfg;
   auto kern = attn_tc_pair_kernel<OUT_FP32>;
-  static int configured_mask = 0;  // per-device bit (devices < 32)
-  static int max_clusters[32] = {};
+  // Per-device set-up (the shared-memory attribute is a per-device setting,
+  // and the cluster occupancy is queried once per device), shared by host
+  // threads under a lock.
+  static std::mutex mu;
+  static bool configured[MAX_DEVICES] = {};
+  static int max_clusters[MAX_DEVICES] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -809,21 +817,25 @@ cudaError_t launch_pair(const AttnArgs& a, const void* tq, const void* tk, const
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!(configured_mask & (1 << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    max_clusters[dev & 31] = n;
-    configured_mask |= 1 << (dev & 31);
+  int clusters = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+      if (e != cudaSuccess) return e;
+      int sms = 0;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n < 1) return cudaErrorInvalidConfiguration;
+      max_clusters[dev] = n;
+      configured[dev] = true;
+    }
+    clusters = max_clusters[dev];
   }
-  int clusters = max_clusters[dev & 31];
   if (n_pairs_hint > 0 && n_pairs_hint < clusters) clusters = n_pairs_hint;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   CUtensorMap mq, mk, mv;

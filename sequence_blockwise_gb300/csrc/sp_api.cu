@@ -20,7 +20,7 @@ namespace {
 
 using sp::AttnArgs;
 
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = sp::MAX_DEVICES;
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s of GPU time per wait
 
 std::mutex g_mu;
@@ -237,7 +237,8 @@ sp_status sp_packed_attention_ex(const void* q, const void* k, const void* v, vo
   if (!device_state(&err, &sms)) return SP_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int rpu = dtype == SP_DTYPE_BF16 ? sp::TC_ROWS_PER_UNIT : sp::SIMT_ROWS_PER_UNIT;
-  cudaError_t e = sp::launch_prep(items_dev, item_heads_dev, n_items, T, Hq, Hkv, rpu, workspace, err, st);
+  cudaError_t e = sp::launch_prep(items_dev, item_heads_dev, n_items, T, Hq, Hkv, rpu, workspace, err,
+                                  cu_seqlens_dev, ndocs, causal, st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
   AttnArgs a = base_args(q, k, v, o, lse, T, Hq, Hkv, d, cu_seqlens_dev, ndocs, causal, scale, err);
   const sp::WsLayout L = sp::ws_layout(n_items);
@@ -319,12 +320,13 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   float* nlse2 = reinterpret_cast<float*>(ws + L.off_nlse2);
   float* dqacc = reinterpret_cast<float*>(ws + L.off_dqacc);
   int32_t* unit_counter = reinterpret_cast<int32_t*>(ws) + sp::WS_BWD_COUNTER;
+  int32_t* status = reinterpret_cast<int32_t*>(ws) + sp::WS_STATUS;
 
   const long long warps = static_cast<long long>(T) * Hq;
   long long g = (warps + 7) / 8;
   if (g > static_cast<long long>(sms) * 16) g = static_cast<long long>(sms) * 16;
-  cudaError_t e = sp::launch_bwd_rowdot(o, dout, lse, ndsc, nlse2, dqacc, unit_counter, T, Hq, d, scale,
-                                        static_cast<int>(g), st);
+  cudaError_t e = sp::launch_bwd_rowdot(o, dout, lse, ndsc, nlse2, dqacc, unit_counter, status,
+                                        cu_seqlens_dev, ndocs, err, T, Hq, d, scale, static_cast<int>(g), st);
   if (e != cudaSuccess) return SP_ERR_CUDA;
 
   sp::BwdArgs b;
@@ -335,6 +337,7 @@ sp_status sp_packed_attention_backward(const void* q, const void* k, const void*
   b.nlse2 = nlse2;
   b.unit_counter = unit_counter;
   b.dqacc = dqacc;
+  b.status = status;
   b.dq = dq;
   b.dk = dk;
   b.dv = dv;

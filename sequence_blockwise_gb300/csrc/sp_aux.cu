@@ -38,9 +38,31 @@ __device__ __forceinline__ void item_heads_of(const int32_t* heads, int i, int H
   }
 }
 
+// Does the item hold at least one (query, key) pair the document and causal
+// masks allow? The documents that meet both its Q range and its key range are
+// those from the later of the two ranges' first documents to the earlier of
+// their last ones; the first with a valid pair ends the search. Every index
+// stays in [0, nd] whatever cu holds.
+__device__ bool item_has_pair(const int32_t* cu, int nd, int qb, int qe, int kb, int ke, int causal) {
+  if (qb >= qe || kb >= ke) return false;
+  const int d0 = max(doc_of(cu, nd, qb), doc_of(cu, nd, kb));
+  const int d1 = min(doc_of(cu, nd, qe - 1), doc_of(cu, nd, ke - 1));
+  for (int d = d0; d <= d1; ++d) {
+    const int ds = __ldg(cu + d), de = __ldg(cu + d + 1);
+    const int q0 = max(qb, ds), q1 = min(qe, de), k0 = max(kb, ds), k1 = min(ke, de);
+    if (q0 < q1 && k0 < k1 && (!causal || k0 <= q1 - 1)) return true;
+  }
+  return false;
+}
+
+// Largest number of groups the set-up kernel orders and checks for overlap
+// (the checks are quadratic in the group count); longer lists are rejected.
+constexpr int MAX_GROUPS = 8192;
+
 __global__ void __launch_bounds__(1024)
 prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads, int n, int T, int Hq,
-            int Hkv, int rpu, int32_t* ws, unsigned* err) {
+            int Hkv, int rpu, int32_t* ws, unsigned* err, const int32_t* __restrict__ cu, int ndocs,
+            int causal) {
   __shared__ long long scan_tmp[1024];
   __shared__ int bad;
   __shared__ int any_sorted;
@@ -57,6 +79,13 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
   }
   __syncthreads();
 
+  // The packing descriptor the masks come from: cu[0] = 0, strictly
+  // increasing, cu[ndocs] = T (documents never overlap or run past the
+  // sequence; HSAP abstract: no cross-contamination between packed documents).
+  for (int i = tid; i <= ndocs; i += 1024) {
+    const int c = __ldg(cu + i);
+    if ((i == 0 && c != 0) || (i == ndocs && c != T) || (i < ndocs && c >= __ldg(cu + i + 1))) bad = 1;
+  }
   const int chunk = (n + 1023) / 1024;
   const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
   const int G = Hq / Hkv;
@@ -74,6 +103,11 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
     const sp_item it = items[i];
     if (!(0 <= it.q_begin && it.q_begin < it.q_end && it.q_end <= T && 0 <= it.kv_begin &&
           it.kv_begin <= it.kv_end && it.kv_end <= T))
+      bad = 1;
+    // Every item holds a valid pair under these masks, as a pruned schedule
+    // built from the same cu_seqlens does; an item that does not means the
+    // device cu_seqlens differs from the one the schedule was built from.
+    else if (!item_has_pair(cu, ndocs, it.q_begin, it.q_end, it.kv_begin, it.kv_end, causal))
       bad = 1;
     int h0, h1;
     item_heads_of(heads, i, Hq, h0, h1);
@@ -142,7 +176,8 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
   __syncthreads();
 
   // Largest estimated cost first (ties keep schedule order).
-  const bool sorted = nseg <= 8192;
+  if (tid == 0 && nseg > MAX_GROUPS) bad = 1;
+  const bool sorted = nseg <= MAX_GROUPS;
   for (int s = tid; s < nseg; s += 1024) {
     int rank = s;
     if (sorted) {
@@ -159,7 +194,7 @@ prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads
 
   // The (Q range x head range) rectangles of different groups must not
   // overlap (each output row of each head is written by exactly one group).
-  if (nseg <= 8192) {
+  if (nseg <= MAX_GROUPS) {
     for (int s = tid; s < nseg; s += 1024) {
       const int a0 = segs[s].q_lo, a1 = segs[s].q_hi, g0 = segs[s].h_lo, g1 = segs[s].h_hi;
       for (int t2 = s + 1; t2 < nseg; ++t2)
@@ -308,9 +343,9 @@ __global__ void wait_selftest_kernel(unsigned long long timeout_ns, unsigned* er
 
 cudaError_t launch_prep(const sp_item* items, const int32_t* item_heads, int64_t n_items, int32_t T,
                         int32_t Hq, int32_t Hkv, int32_t rows_per_unit, void* workspace, unsigned* err,
-                        cudaStream_t st) {
+                        const int32_t* cu, int32_t ndocs, int32_t causal, cudaStream_t st) {
   prep_kernel<<<1, 1024, 0, st>>>(items, item_heads, static_cast<int>(n_items), T, Hq, Hkv, rows_per_unit,
-                                  static_cast<int32_t*>(workspace), err);
+                                  static_cast<int32_t*>(workspace), err, cu, ndocs, causal ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -10,6 +10,10 @@
 
 namespace sp {
 
+// Devices a process may use the library on (per-device state is kept in
+// arrays of this size; larger device ids are rejected).
+constexpr int MAX_DEVICES = 64;
+
 // Error bits recorded in the per-device error word.
 enum : unsigned { ERR_TIMEOUT_BIT = 1u, ERR_INTERNAL_BIT = 2u };
 
@@ -76,6 +80,7 @@ struct BwdArgs {
   const float* nlse2;  // [Hq][T] -LSE_i * log2(e)
   int32_t* unit_counter;  // fused kernel's work-unit queue (zeroed by the row-dot kernel)
   float* dqacc;       // fp32 [T][Hq][d] dQ accumulator (zeroed by the row-dot kernel)
+  int32_t* status;    // nonzero when the row-dot kernel found cu_seqlens invalid (nothing is written)
   void* dq;           // bf16 [T][Hq][d]
   void* dk;           // bf16 [T][Hkv][d]
   void* dv;           // bf16 [T][Hkv][d]
@@ -86,7 +91,7 @@ struct BwdArgs {
 // ranges; a range must cover whole key/value-head groups or lie inside one.
 cudaError_t launch_prep(const sp_item* items, const int32_t* item_heads, int64_t n_items, int32_t T,
                         int32_t Hq, int32_t Hkv, int32_t rows_per_unit, void* workspace, unsigned* err,
-                        cudaStream_t st);
+                        const int32_t* cu, int32_t ndocs, int32_t causal, cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, const void* tmap_q, const void* tmap_k,
                            const void* tmap_v, int grid, cudaStream_t st);
@@ -98,7 +103,8 @@ cudaError_t launch_attn_tc_pair(const AttnArgs& a, const void* tmap_q, const voi
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
                              int32_t rows, int32_t Hq, int32_t d, int grid, cudaStream_t st);
 cudaError_t launch_bwd_rowdot(const void* o, const void* dout, const float* lse, float* ndsc, float* nlse2,
-                              float* dqacc, int32_t* unit_counter, int T, int Hq, int d, float scale, int grid,
+                              float* dqacc, int32_t* unit_counter, int32_t* status, const int32_t* cu,
+                              int ndocs, unsigned* err, int T, int Hq, int d, float scale, int grid,
                               cudaStream_t st);
 // The fused dK/dV/dQ kernel (key/value tiles stationary, dQ reduced into
 // dqacc), then dQ rounded from dqacc to bf16.

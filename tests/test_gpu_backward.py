@@ -23,11 +23,14 @@ error must stay below 1e-2.
 
 Full-size workloads (the benchmark's launch): dQ at sampled rows and dK, dV
 at sampled keys from the oracle's sampled form (rows at document, chunk and
-tile edges; keys whose attending queries the oracle can afford), checked by
-the same Frobenius bound and max|error| <= 2e-2 max|ref| over the sample, plus
-two identities that hold at any size, per document and key/value head:
-sum_j dV_j = sum_i sum_(h in group) dO_ih (softmax rows sum to one) and
-sum_j dK_j = 0 (sum_j dS_ij = 0 for every row)."""
+tile edges; keys whose attending queries the oracle can afford). Every sampled
+element is held to the same rounding envelope as the small cases, computed for
+the sampled positions only, and each sampled tensor to the same Frobenius
+bound and max|error| <= 2e-2 max|ref|; plus two identities that hold at any
+size, per document and key/value head: sum_j dV_j = sum_i sum_(h in group)
+dO_ih (softmax rows sum to one) and sum_j dK_j = 0 (sum_j dS_ij = 0 for every
+row). The tolerances are this file's own derivation (the benchmark spec's figures
+cover the forward only): the envelope above, 1e-2 relative Frobenius."""
 import math
 
 import numpy as np
@@ -133,16 +136,21 @@ def test_backward_matches_oracle(case):
 
 
 def test_backward_deterministic_and_schedule_invariant():
-    """Two runs give identical bits; RING and TASP schedules give the same dK
-    and dV (computed over the mask) and dQ within rounding."""
+    """Two runs give identical dK and dV bits (each is summed in a fixed order)
+    and dQ equal up to the rounding of its fp32 reduction order; RING and TASP
+    schedules give the same dK and dV (computed over the mask) and dQ within
+    rounding."""
     torch = _torch()
     T, docs, Hq, Hkv, d = 1000, [1, 1, 500, 498], 8, 2, 128
     cu = wl.cu_from_lengths(docs)
     q, k, v, do = _inputs(T, Hq, Hkv, d, 7)
     a = _fwd_bwd(q, k, v, do, cu, True, sb.SP_SCHED_TASP, 8)
     b = _fwd_bwd(q, k, v, do, cu, True, sb.SP_SCHED_TASP, 8)
-    for x, y in zip(a[2:], b[2:]):
-        assert torch.equal(x, y)
+    assert torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])
+    # One bf16 step of the larger value at most, where fp32 sums in another
+    # order round to the other side of a bf16 midpoint.
+    gap = (a[2].float() - b[2].float()).abs()
+    assert bool((gap <= 2.0 ** -7 * torch.maximum(a[2].float().abs(), b[2].float().abs()) + 1e-30).all())
     c = _fwd_bwd(q, k, v, do, cu, True, sb.SP_SCHED_RING, 2)
     for x, y in zip(a[2:], c[2:]):
         assert float((x.float() - y.float()).abs().max()) <= 2e-2 * float(x.float().abs().max())
@@ -248,6 +256,74 @@ def _pick_samples(w, cu):
     return np.array(sorted(qrows), dtype=np.int64), np.array(sorted(set(krows)), dtype=np.int64)
 
 
+def _row_stats(qr, kd, vd, dor, scale, valid):
+    """Full-row quantities of query rows qr, dor [r, Hkv, G, d] (query head
+    g G + x) over a document's keys kd, vd [n, Hkv, d], valid [r, n] bool:
+    P, dP [r, Hkv, G, n] and D, A [r, Hkv, G], in float64."""
+    torch = _torch()
+    sc = torch.einsum("rgxc,ngc->rgxn", qr, kd) * scale
+    sc = sc.masked_fill(~valid[:, None, None, :], float("-inf"))
+    p = torch.softmax(sc, -1)
+    o = torch.einsum("rgxn,ngc->rgxc", p, vd)
+    D = (dor * o).sum(-1)
+    A = (dor.abs() * o.abs()).sum(-1)
+    dp = torch.einsum("rgxc,ngc->rgxn", dor, vd)
+    return p, dp, D, A
+
+
+def _weights(p, dp, D, A):
+    ds = p * (dp - D[..., None])
+    return ds.abs() + p * (dp.abs() + D.abs()[..., None] + A[..., None])
+
+
+def _sampled_envelopes(q, k, v, do, cu, causal, scale, qrows, krows, block=8):
+    """The rounding envelopes of _envelopes at the sampled dQ rows and dK/dV
+    keys only, in float64 (on the device, in blocks of `block` query rows)."""
+    torch = _torch()
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    cu = np.asarray(cu, dtype=np.int64)
+    dev = q.device
+    grp = lambda x: x.double().reshape(x.shape[0], Hkv, G, d)
+    m_dq = np.zeros((len(qrows), Hq, d))
+    m_dk = np.zeros((len(krows), Hkv, d))
+    m_dv = np.zeros((len(krows), Hkv, d))
+    qdoc = np.searchsorted(cu, qrows, side="right") - 1
+    kdoc = np.searchsorted(cu, krows, side="right") - 1
+    for di in np.unique(np.concatenate([qdoc, kdoc])):
+        a, b = int(cu[di]), int(cu[di + 1])
+        kd, vd = k[a:b].double(), v[a:b].double()
+        keys = torch.arange(a, b, device=dev)
+        for n_i in np.nonzero(qdoc == di)[0]:
+            i = int(qrows[n_i])
+            valid = (keys <= i)[None, :] if causal else torch.ones((1, b - a), dtype=torch.bool, device=dev)
+            p, dp, D, A = _row_stats(grp(q[i:i + 1]), kd, vd, grp(do[i:i + 1]), scale, valid)
+            w = _weights(p, dp, D, A)
+            m_dq[n_i] = (scale * torch.einsum("rgxn,ngc->rgxc", w, kd.abs())).reshape(Hq, d).cpu().numpy()
+        sel = np.nonzero(kdoc == di)[0]
+        if len(sel) == 0:
+            continue
+        cols = torch.from_numpy(krows[sel] - a).to(dev)
+        r0 = int(krows[sel].min()) if causal else a  # the first query attending these keys
+        acc_k = torch.zeros((len(sel), Hkv, d), dtype=torch.float64, device=dev)
+        acc_v = torch.zeros((len(sel), Hkv, d), dtype=torch.float64, device=dev)
+        for s0 in range(r0, b, block):
+            s1 = min(b, s0 + block)
+            rows = torch.arange(s0, s1, device=dev)
+            valid = (keys[None, :] <= rows[:, None]) if causal else \
+                torch.ones((s1 - s0, b - a), dtype=torch.bool, device=dev)
+            qr, dor = grp(q[s0:s1]), grp(do[s0:s1])
+            p, dp, D, A = _row_stats(qr, kd, vd, dor, scale, valid)
+            p, dp = p[..., cols], dp[..., cols]
+            w = _weights(p, dp, D, A)
+            acc_k += scale * torch.einsum("rgxk,rgxc->kgc", w, qr.abs())
+            acc_v += torch.einsum("rgxk,rgxc->kgc", p, dor.abs())
+        m_dk[sel] = acc_k.cpu().numpy()
+        m_dv[sel] = acc_v.cpu().numpy()
+    return m_dq, m_dk, m_dv
+
+
 BF16_WORKLOADS = [w for w in wl.WORKLOADS if w.dtype == "bf16"]
 
 
@@ -283,12 +359,17 @@ def test_backward_workload_parity(w):
                                               host_inputs(do), cu, w.causal, qrows, krows)
     qi = torch.from_numpy(qrows).cuda()
     ki = torch.from_numpy(krows).cuda()
-    for name, got, ref in (("dq", dq[qi], rq), ("dk", dk[ki], rk), ("dv", dv[ki], rv)):
+    env = _sampled_envelopes(q, k, v, do, cu, w.causal, 1.0 / math.sqrt(w.d), qrows, krows)
+    for name, got, ref, mm in (("dq", dq[qi], rq, env[0]), ("dk", dk[ki], rk, env[1]),
+                               ("dv", dv[ki], rv, env[2])):
         if ref.shape[0] == 0:
             continue
         g = got.double().cpu().numpy()
         err = float(np.abs(g - ref).max())
         mx = float(np.abs(ref).max())
         fro = _rel_fro(g, ref)
-        print(f"{w.name} {name}: {g.shape[0]} samples max|err|={err:.3e} max|ref|={mx:.3e} rel_fro={fro:.3e}")
+        worst = float(np.max(np.abs(g - ref) / (2.0 ** -7 * mm + 2.0 ** -8 * np.abs(ref) + 1e-6)))
+        print(f"{w.name} {name}: {g.shape[0]} samples max|err|={err:.3e} max|ref|={mx:.3e} "
+              f"rel_fro={fro:.3e} worst err/envelope={worst:.3f}")
+        assert worst <= 1.0, (name, worst)
         assert err <= REL_MAX_SAMPLED * mx and fro <= REL_FRO, (name, err, mx, fro)

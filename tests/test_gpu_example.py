@@ -1,8 +1,6 @@
-"""The Python example in README.md runs as printed, and its outputs match the
-fp64 oracle on sampled rows (document edges, tile edges and random rows)."""
-import os
-import re
-
+"""The binding's example (sequence_blockwise_gb300/example.py) runs, and its
+outputs match the fp64 oracle on sampled rows (document edges, tile edges and
+random rows)."""
 import numpy as np
 import pytest
 
@@ -10,17 +8,13 @@ from gpu_util import TOL_BF16_LSE, TOL_BF16_O, max_errs, oracle_rows, sample_row
 
 pytestmark = pytest.mark.gpu
 
-README = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "README.md")
 
-
-def test_readme_python_example():
+def test_example_runs_and_matches_oracle():
     import torch
-    block = re.search(r"```python\n(.*?)```", open(README).read(), re.S).group(1)
-    torch.manual_seed(0)
-    ns = {}
-    exec(compile(block, "README.md", "exec"), ns)
-    q, k, v, o, lse, cu = ns["q"], ns["k"], ns["v"], ns["o"], ns["lse"], ns["cu"]
-    dq, dk, dv = ns["dq"], ns["dk"], ns["dv"]
+    from sequence_blockwise_gb300 import example
+    out = example.run()
+    q, k, v, o, lse, cu = (out[n] for n in ("q", "k", "v", "o", "lse", "cu"))
+    dq, dk, dv = out["dq"], out["dk"], out["dv"]
     T, Hq, d = q.shape
     assert o.shape == q.shape and o.dtype == torch.bfloat16
     assert lse.shape == (Hq, T) and lse.dtype == torch.float32
