@@ -8,11 +8,17 @@ FLOP = 4 * d * Hq * (valid query-key pairs).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun every rank runs its own copy of the workload (independent
-problems, no collective on the data path: weak scaling); the timed region is
-bracketed by a barrier and device synchronisation, and its maximum over ranks
-is reported. `--impl reference` times the fp64 CPU oracle on a bounded sample
-of the same workload.
+Under torchrun the virtual sequence-parallel ranks are split over the GPUs
+(default, `--split ranks`): GPU g runs the schedule items of the virtual ranks
+r with r mod N = g (their Q chunks against the K/V chunks their steps visit),
+with K and V resident on every GPU before the timed region, so no data crosses
+GPUs inside it; `value` is the whole workload's FLOP over the slowest GPU's
+time (strong scaling). `--split replicas` runs an independent full copy per GPU
+(weak scaling). The timed region is bracketed by a barrier and device
+synchronisation, and its maximum over ranks is reported. With N = 1 the line
+also carries `per_workload`: forward (and backward) time of every workload.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload.
 """
 from __future__ import annotations
 
@@ -165,6 +171,19 @@ def dist_barrier(world: int):
         dist.barrier()
 
 
+def dist_gather(x: float, world: int) -> list:
+    """Every rank's value of x, in rank order."""
+    if world == 1:
+        return [x]
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    out = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(out, t)
+    return [float(o.item()) for o in out]
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 def oracle_sample(w, cu, seconds: float, seed: int = 0):
@@ -199,6 +218,103 @@ def oracle_sample(w, cu, seconds: float, seed: int = 0):
     return flop, elapsed, nrows, threads
 
 
+# ------------------------------------------------------------------ SP split
+
+def split_items(items, world: int, gpu: int):
+    """The schedule items GPU `gpu` of `world` runs: those of the virtual ranks
+    r with r mod world == gpu (each virtual rank's Q chunk and its chunk-visit
+    steps stay on one GPU, as a sequence-parallel rank's do). Returns the item
+    rows in schedule order."""
+    items = np.asarray(items)
+    return np.ascontiguousarray(items[(items[:, 0] % world) == gpu])
+
+
+def row_intervals(items):
+    """The union of the items' Q ranges as sorted, disjoint [a, b) intervals:
+    the output rows a GPU writes."""
+    spans = sorted({(int(it[3]), int(it[4])) for it in np.asarray(items)})
+    out = []
+    for a, b in spans:
+        if out and a <= out[-1][1]:
+            out[-1][1] = max(out[-1][1], b)
+        else:
+            out.append([a, b])
+    return [(a, b) for a, b in out]
+
+
+def owned_chunks(kind: int, P: int, T: int, rank: int):
+    """The Q chunks virtual rank `rank` owns (equal chunking): RING and TASP,
+    chunk r of P (the first T mod P get one more token); ZIGZAG, chunks r and
+    2P-1-r of 2P equal chunks."""
+    if kind == 1:  # zigzag
+        c = T // (2 * P)
+        return sorted([(rank * c, (rank + 1) * c), ((2 * P - 1 - rank) * c, (2 * P - rank) * c)])
+    base, extra = divmod(T, P)
+    a = rank * base + min(rank, extra)
+    return [(a, a + base + (1 if rank < extra else 0))]
+
+
+# ------------------------------------------------------------------ tile work
+
+def tile_work(items, cu, causal: bool, T: int, rows_per_unit: int = 256):
+    """Executed (query, key) tile area of the tensor-core forward for one query
+    head, from the same walk the kernels do: items grouped by (rank, Q range);
+    each unit is two 128-row Q tiles; an item's key range is clipped to the keys
+    some row of the unit may attend (its rows' documents; up to its last row
+    when causal) and walked in 128-key tiles from the clipped start; when some
+    group holds items that are not whole 128-key tiles long, every group walks
+    its items in key order and joins contiguous clipped ranges; a (Q tile, key
+    tile) pair costs 128 x 128 unless it holds no valid pair for the tile's rows
+    (skipped). Divided by the valid pairs, this is the forward's tile work."""
+    items = np.asarray(items)
+    cu = np.asarray(cu, dtype=np.int64)
+    doc = lambda t: int(np.searchsorted(cu, t, side="right") - 1)
+    groups, start = [], 0
+    for i in range(1, len(items) + 1):
+        if i == len(items) or tuple(items[i, [0, 3, 4]]) != tuple(items[start, [0, 3, 4]]):
+            groups.append((start, i))
+            start = i
+    ordered = any(((items[a:b, 6] - items[a:b, 5]) % 128 != 0).any() and b - a <= 2048 for a, b in groups)
+    work = 0
+    for a, b in groups:
+        g = items[a:b]
+        if ordered and ((g[:, 6] - g[:, 5]) % 128 != 0).any() and b - a <= 2048:
+            g = g[np.argsort(g[:, 5], kind="stable")]
+        q_lo, q_hi = int(g[0, 3]), int(g[0, 4])
+        for q0 in range(q_lo, q_hi, rows_per_unit):
+            tiles = []
+            for i in range(2):
+                qa, qb = q0 + 128 * i, min(q0 + 128 * (i + 1), q_hi)
+                if qa < qb:
+                    tiles.append((qa, qb, int(cu[doc(qa)]), int(cu[doc(qb - 1) + 1])))
+            if not tiles:
+                continue
+            lo, hi = tiles[0][2], tiles[-1][3]
+            if causal:
+                hi = min(hi, tiles[-1][1])
+            ranges, j = [], 0
+            while j < len(g):
+                k0, k1 = max(int(g[j, 5]), lo), min(int(g[j, 6]), hi)
+                j += 1
+                while ordered and k0 < k1 and j < len(g):
+                    n0, n1 = max(int(g[j, 5]), lo), min(int(g[j, 6]), hi)
+                    if n0 != k1 or n1 <= n0:
+                        break
+                    k1 = n1
+                    j += 1
+                if k0 < k1:
+                    ranges.append((k0, k1))
+            for k0, k1 in ranges:
+                ka = np.arange(k0, k1, 128, dtype=np.int64)
+                kb = np.minimum(ka + 128, k1)
+                for qa, qb, ds, de in tiles:
+                    skip = (de <= ka) | (kb <= ds)
+                    if causal:
+                        skip |= ka > qb - 1
+                    work += int((~skip).sum()) * 128 * 128
+    return work
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_ours(args, world, rank, local):
@@ -216,10 +332,23 @@ def run_ours(args, world, rank, local):
     o = torch.empty_like(q)
     lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 2  # set-up kernel + persistent attention kernel
+    # Sequence-parallel split (default): GPU g runs the items of the virtual
+    # ranks r with r mod N = g, i.e. their Q chunks against the K/V chunks their
+    # schedule visits; K and V are resident on every GPU before the timed
+    # region, so nothing crosses GPUs inside it. With N = 1 that is the whole
+    # schedule. --split replicas runs an independent full copy per GPU.
+    split = "replicas" if (world > 1 and args.split == "replicas") else "ranks"
+    my_items = split_items(att.items, world, rank) if split == "ranks" else att.items
+    n_my = int(len(my_items))
+    my_intervals = row_intervals(my_items) if n_my else []
+    my_flop = 4.0 * w.d * w.Hq * sum(valid_pairs_range(cu, w.causal, it) for it in my_items)
+    my_items_dev = torch.from_numpy(np.ascontiguousarray(my_items)).to(dev) if n_my else None
+    my_ws = torch.empty(sb.sp_packed_attention_workspace_size(max(n_my, 1)), dtype=torch.uint8, device=dev)
+    launches_per_step = 2 if n_my else 0  # set-up kernel + persistent attention kernel
 
     def step():
-        att(q, k, v, o, lse, stream=stream)
+        if n_my:
+            sb.sp_packed_attention(q, k, v, o, lse, att.cu_dev, w.causal, my_items_dev, my_ws, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -246,9 +375,11 @@ def run_ours(args, world, rank, local):
     total_ms = t_start.elapsed_time(t_end)
     per = [a.elapsed_time(b) for a, b in ev]
     sb.sp_check_device_status(stream)
+    gpu_ms = dist_gather(total_ms / args.steps, world)
     total_ms = dist_max(total_ms, world)
     ms_step = total_ms / args.steps
-    value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
+    job_flop = flop if split == "ranks" else world * flop
+    value = job_flop * args.steps / (total_ms * 1e-3) / 1e12
 
     # ---- end to end through the C-ABI with host buffers: every step copies its
     # inputs (Q, K, V, cu_seqlens, items) from pinned host memory and reads its O
@@ -269,10 +400,15 @@ def run_ours(args, world, rank, local):
     od = [torch.empty_like(o) for _ in range(2)]
     ld = [torch.empty_like(lse) for _ in range(2)]
     cud = [torch.empty_like(att.cu_dev) for _ in range(2)]
-    itd = [torch.empty_like(att.items_dev) for _ in range(2)]
-    h2d = (qh.numel() * qh.element_size() + kh.numel() * kh.element_size() +
-           vh.numel() * vh.element_size() + cu_h.numel() * 4 + it_h.numel() * 4)
-    d2h = oh[0].numel() * oh[0].element_size() + lh[0].numel() * lh[0].element_size()
+    itd = [torch.empty_like(att.items_dev) for _ in range(2)]  # holds this GPU's items at the front
+    it_h = torch.from_numpy(np.ascontiguousarray(my_items)).pin_memory() if n_my else it_h
+    row_bytes = w.Hq * w.d * q.element_size()
+    my_rows = sum(b - a for a, b in my_intervals)
+    # Per step: this GPU's Q rows, all of K and V, cu_seqlens and its items in;
+    # its O rows and the LSE out.
+    h2d = (my_rows * row_bytes + kh.numel() * kh.element_size() + vh.numel() * vh.element_size() +
+           cu_h.numel() * 4 + (it_h.numel() * 4 if n_my else 0))
+    d2h = my_rows * row_bytes + lh[0].numel() * lh[0].element_size()
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
@@ -286,21 +422,25 @@ def run_ours(args, world, rank, local):
             with torch.cuda.stream(s_in):
                 if i >= 2:
                     s_in.wait_event(ev_comp[sl])  # step i-2 has finished reading this slot
-                qd[sl].copy_(qh, non_blocking=True)
+                for a, b in my_intervals:
+                    qd[sl][a:b].copy_(qh[a:b], non_blocking=True)
                 kd[sl].copy_(kh, non_blocking=True)
                 vd[sl].copy_(vh, non_blocking=True)
                 cud[sl].copy_(cu_h, non_blocking=True)
-                itd[sl].copy_(it_h, non_blocking=True)
+                if n_my:
+                    itd[sl][:n_my].copy_(it_h, non_blocking=True)
                 ev_in[sl].record(s_in)
             stream.wait_event(ev_in[sl])
             if i >= 2:
                 stream.wait_event(ev_out[sl])  # step i-2's outputs have left this slot
-            sb.sp_packed_attention(qd[sl], kd[sl], vd[sl], od[sl], ld[sl], cud[sl], w.causal, itd[sl],
-                                   att.workspace, stream=stream)
+            if n_my:
+                sb.sp_packed_attention(qd[sl], kd[sl], vd[sl], od[sl], ld[sl], cud[sl], w.causal,
+                                       itd[sl][:n_my], my_ws, stream=stream)
             ev_comp[sl].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[sl])
-                oh[sl].copy_(od[sl], non_blocking=True)
+                for a, b in my_intervals:
+                    oh[sl][a:b].copy_(od[sl][a:b], non_blocking=True)
                 lh[sl].copy_(ld[sl], non_blocking=True)
                 ev_out[sl].record(s_out)
         for sl in range(min(2, n_steps)):
@@ -319,15 +459,18 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     dist_barrier(world)
     e2e_ms = dist_max(e0.elapsed_time(e1), world)
-    e2e_value = world * flop * args.steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = job_flop * args.steps / (e2e_ms * 1e-3) / 1e12
     sb.sp_check_device_status(stream)
-    # The pipelined result equals the device-resident one.
-    e2e_same = bool(torch.equal(oh[(args.steps - 1) % 2], o.cpu())) if args.steps > 0 else True
+    # The pipelined result equals the device-resident one on this GPU's rows.
+    e2e_same = True
+    if args.steps > 0:
+        o_cpu, last = o.cpu(), oh[(args.steps - 1) % 2]
+        e2e_same = all(bool(torch.equal(last[a:b], o_cpu[a:b])) for a, b in my_intervals)
 
     # ---- backward of the same call (dQ, dK, dV), timed on its own after the
     # forward's timed region; reported beside the headline, not in `value`.
     bwd = None
-    if not args.no_backward:
+    if not args.no_backward and world == 1:
         dout = wl.random_normal((w.T, w.Hq, w.d), w.seed + 99, dev, "bf16")
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         att(q, k, v, o, lse, stream=stream)
@@ -360,7 +503,7 @@ def run_ours(args, world, rank, local):
     # 64K full-mask layer's partials over all rows at once, so that the three
     # fp32 O arrays (512 MB each) are far larger than L2.
     merge = None
-    if not args.no_backward:
+    if not args.no_backward and world == 1:
         wm = wl.WORKLOADS[3]
         rows, Hm, dm = wm.T, wm.Hq, wm.d
         o_acc = torch.randn((rows, Hm, dm), dtype=torch.float32, device=dev)
@@ -392,7 +535,7 @@ def run_ours(args, world, rank, local):
     if bwd is not None:
         bwd["frac_of_peak"] = round(bwd["tflops"] / peaks["bf16_tflops"], 4)
     avg_launch_ms = sum(per) / len(per)
-    achieved = flop / (avg_launch_ms * 1e-3) / 1e12
+    achieved = my_flop / (avg_launch_ms * 1e-3) / 1e12 if avg_launch_ms > 0 else 0.0
     traffic = kernel_traffic()
     io_bytes = (q.numel() + k.numel() + v.numel() + o.numel()) * 2 + lse.numel() * 4
 
@@ -407,7 +550,7 @@ def run_ours(args, world, rank, local):
             "warmup": max(args.warmup, 3),
             "ms_per_step": round(ms_step, 4),
             "higher_is_better": True,
-            "scaling": "weak",
+            "scaling": "strong" if split == "ranks" else "weak",
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) Q/K/V rounded to bf16; no dataset or weights)",
@@ -415,10 +558,16 @@ def run_ours(args, world, rank, local):
                 "workload": w.name, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
                 "causal": w.causal, "docs": int(len(cu) - 1), "schedule": sched_name(w.kind),
                 "P_virtual": w.P, "n_items": int(len(att.items)), "valid_pairs": pairs,
-                "flop_per_step": flop, "parallelism": f"weak x{world} (independent problems)",
+                "flop_per_step": job_flop,
+                "parallelism": (f"sp split x{world}: GPU g runs the virtual ranks r with r mod {world} = g "
+                                "(their Q chunks and chunk-visit steps); K/V resident on every GPU; "
+                                "no collective" if split == "ranks" else
+                                f"weak x{world} (independent problems)"),
                 "l2": f"inputs+outputs {io_bytes / 2**20:.0f} MiB > L2 129 MiB; no flush",
             },
             "pct_of_peak": round(100.0 * value / world / peaks["bf16_tflops"], 2),
+            "split": {"mode": split, "gpu_ms_per_step": [round(x, 4) for x in gpu_ms],
+                      "gpu_ms_max": round(max(gpu_ms), 4), "gpu_ms_sum": round(sum(gpu_ms), 4)},
             "roofline": {
                 "bound": "tensor", "achieved": round(achieved, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -438,6 +587,95 @@ def run_ours(args, world, rank, local):
             "secondary_roofline": merge,
         }
     return result, w, cu
+
+
+def per_workload_report(args, local):
+    """Forward time of every workload on this GPU (and the backward's for the
+    bf16 ones), each workload's full schedule in one sp_packed_attention call,
+    CUDA events around each call, median over the calls. For the 64K full-mask
+    layer also the API path: one sp_partial_attn per schedule item into fp32
+    partials and an sp_lse_merge per further item of a Q range."""
+    import torch
+    import sequence_blockwise_gb300 as sb
+    from sequence_blockwise_gb300 import workloads as wl
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peak = read_peaks()["bf16_tflops"]
+
+    def timed(fn, n, warm):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b))
+        sb.sp_check_device_status(stream)
+        return float(np.median(ts))
+
+    out = []
+    for w in wl.WORKLOADS:
+        big = w.T >= 262144
+        cu = wl.cu_seqlens(w)
+        pairs = valid_pairs(cu, w.causal)
+        flop = 4.0 * w.d * w.Hq * pairs
+        q, k, v = wl.make_qkv(w, dev)
+        att = sb.PackedAttention(cu, w.causal, w.kind, w.P, w.Hq, seed=w.seed, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
+        f_ms = timed(lambda: att(q, k, v, o, lse, stream=stream), 2 if big else 5, 1 if big else 3)
+        e = {"workload": w.name, "dtype": w.dtype, "schedule": sched_name(w.kind), "P_virtual": w.P,
+             "n_items": int(len(att.items)), "valid_pairs": pairs, "forward_ms": round(f_ms, 4),
+             "forward_tflops": round(flop / (f_ms * 1e-3) / 1e12, 2),
+             "forward_kernel": fwd_kernel_name(w) if w.dtype == "bf16" else f"attn_simt_kernel<{w.d}> (fp32)"}
+        if w.dtype == "bf16":
+            e["forward_frac_of_peak"] = round(flop / (f_ms * 1e-3) / 1e12 / peak, 4)
+            e["tile_work_over_valid_pairs"] = round(tile_work(att.items, cu, w.causal, w.T) / pairs, 4)
+            dout = wl.random_normal((w.T, w.Hq, w.d), w.seed + 99, dev, "bf16")
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            b_ms = timed(lambda: att.backward(q, k, v, o, lse, dout, dq, dk, dv, stream=stream),
+                         1 if big else 3, 1 if big else 2)
+            e["backward_ms"] = round(b_ms, 4)
+            e["backward_tflops"] = round(2.5 * flop / (b_ms * 1e-3) / 1e12, 2)
+            e["backward_frac_of_peak"] = round(2.5 * flop / (b_ms * 1e-3) / 1e12 / peak, 4)
+            del dout, dq, dk, dv
+        else:
+            e["forward_frac_of_peak"] = None  # fp32 on CUDA cores, launch bound at this size
+        if w.name.startswith("noncausal"):
+            items = att.items
+            groups = {}
+            for it in items:
+                groups.setdefault((int(it[0]), int(it[3]), int(it[4])), []).append(it)
+            rows = max(int(it[4] - it[3]) for it in items)
+            acc = [torch.empty((rows, w.Hq, w.d), dtype=torch.float32, device=dev) for _ in range(2)]
+            accl = [torch.empty((w.Hq, rows), dtype=torch.float32, device=dev) for _ in range(2)]
+
+            def api():
+                for (_, qa, qb), its in groups.items():
+                    n = qb - qa
+                    oa, la = acc[0][:n], accl[0][:, :n]
+                    op, lp = acc[1][:n], accl[1][:, :n]
+                    for j, it in enumerate(its):
+                        dst_o, dst_l = (oa, la) if j == 0 else (op, lp)
+                        sb.sp_partial_attn(q, k, v, dst_o, dst_l, qa, qb, int(it[5]), int(it[6]), att.cu_dev,
+                                           w.causal, stream=stream)
+                        if j > 0:
+                            sb.sp_lse_merge(oa, la, op, lp, stream=stream)
+
+            a_ms = timed(api, 2, 1)
+            e["api_path"] = {"ms": round(a_ms, 4), "tflops": round(flop / (a_ms * 1e-3) / 1e12, 2),
+                             "launches": int(len(items) + len(items) - len(groups)),
+                             "what": "one sp_partial_attn per item (fp32 partials) + sp_lse_merge per "
+                                     "further item of a Q range"}
+            del acc, accl
+        out.append(e)
+        del q, k, v, o, lse, att
+        torch.cuda.empty_cache()
+    return out
 
 
 def kernel_only(args, local):
@@ -600,6 +838,11 @@ def main():
                     help="per-virtual-rank device time of the chunking policies (one JSON line each)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only W warm-up + K device-resident steps (driver for ncu captures)")
+    ap.add_argument("--split", choices=["ranks", "replicas"], default="ranks",
+                    help="with N > 1 GPUs: split the virtual ranks over the GPUs (strong scaling) or run "
+                         "one independent copy per GPU (weak scaling)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per_workload report (forward/backward of every workload)")
     ap.add_argument("--workload", default=None,
                     help="with --kernel-only: workload name (default: the 32K-token layer)")
     args = ap.parse_args()
@@ -649,6 +892,8 @@ def main():
         return
 
     result, w, cu = run_ours(args, world, rank, local)
+    if rank == 0 and world == 1 and not args.no_per_workload:
+        result["per_workload"] = per_workload_report(args, local)
     if rank == 0:
         if args.no_cpu_baseline or world > 1:
             result["cpu_baseline"] = None
