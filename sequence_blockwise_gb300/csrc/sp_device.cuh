@@ -318,6 +318,82 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
   return d;
 }
 
+// ---------------------------------------------------------------------------
+// Clusters (pairs of CTAs on the two SMs of a TPC).
+
+__device__ __forceinline__ uint32_t cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_idx() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t n_clusters() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive with no ordering of this thread's memory accesses (a bare signal).
+__device__ __forceinline__ void arrive_relaxed_cluster(uint32_t cl_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(cl_bar) : "memory");
+}
+__device__ __forceinline__ void arrive_cluster(uint32_t cl_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cl_bar) : "memory");
+}
+__device__ __forceinline__ void st_cluster(uint32_t cl_addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(cl_addr), "r"(v) : "memory");
+}
+// Arrive on a barrier of either CTA (CTA-scope release: what it orders is
+// tensor-memory traffic, fenced by tcgen05.wait::st and fence::before_thread_sync).
+__device__ __forceinline__ void arrive_remote(uint32_t cl_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cl_bar) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Barrier waits with cluster-scope acquire, for barriers whose completion
+// carries data another CTA of the cluster stored into this CTA's shared memory
+// (unit slots, exchanged tiles). Hand-offs that order only TMA, tensor-memory
+// and MMA traffic use the CTA-scope waits above: a cluster-scope acquire or
+// release there costs a memory barrier on every tile.
+__device__ __forceinline__ bool try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait (as mbar_wait_bounded in sp_device.cuh).
+__device__ __forceinline__ bool wait_cl(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
+                                        unsigned* err, volatile int* abort) {
+  if (try_wait_cl(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (try_wait_cl(bar, parity)) return true;
+    if ((++spins & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        atomicOr(err, ERR_TIMEOUT_BIT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulate:
 // D format F32 at [4,6), A/B format BF16 at [7,10)/[10,13), A/B major at
 // bits 15/16 (0 = K-major, 1 = MN-major), N>>3 at [17,23), M>>4 at [24,29).
