@@ -182,16 +182,8 @@ __device__ __forceinline__ void store_zero_row_bf16(uint16_t* dst, int n) {
   for (int j = 0; j < n; j += 8) *reinterpret_cast<uint4*>(dst + j) = make_uint4(0, 0, 0, 0);
 }
 
-// Loads 64 consecutive TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld64(uint32_t t, uint32_t (&x)[64]) {
-  uint32_t a[32];
-  tmem_ld32_sync(t, a);
-#pragma unroll
-  for (int c = 0; c < 32; ++c) x[c] = a[c];
-  tmem_ld32_sync(t + 32, a);
-#pragma unroll
-  for (int c = 0; c < 32; ++c) x[32 + c] = a[c];
-}
+// Loads 64 consecutive TMEM columns of this thread's lane (one load, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t t, uint32_t (&x)[64]) { tmem_ld64_sync(t, x); }
 
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t d;
@@ -338,12 +330,17 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restr
     const int t = static_cast<int>(w / Hq), h = static_cast<int>(w % Hq);
     const uint16_t* po = o + static_cast<size_t>(w) * d;
     const uint16_t* pd = dout + static_cast<size_t>(w) * d;
+    // 16-byte loads: lane l reads elements [8 l, 8 l + 8) (d = 128: 16 lanes, d = 64: 8).
     float acc = 0.f;
-    for (int c = 2 * lane; c < d; c += 64) {
-      const uint32_t a = *reinterpret_cast<const uint32_t*>(po + c);
-      const uint32_t b = *reinterpret_cast<const uint32_t*>(pd + c);
-      acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
-      acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
+    for (int c = 8 * lane; c < d; c += 256) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(po + c));
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(pd + c));
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc = fmaf(__uint_as_float(av[i] << 16), __uint_as_float(bv[i] << 16), acc);
+        acc = fmaf(__uint_as_float(av[i] & 0xffff0000u), __uint_as_float(bv[i] & 0xffff0000u), acc);
+      }
     }
     float4* zq = reinterpret_cast<float4*>(dqacc + static_cast<size_t>(w) * d);
     for (int c = lane; c < d / 4; c += 32) zq[c] = make_float4(0.f, 0.f, 0.f, 0.f);
