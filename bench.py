@@ -537,7 +537,9 @@ def run_ours(args, world, rank, local):
     avg_launch_ms = sum(per) / len(per)
     achieved = my_flop / (avg_launch_ms * 1e-3) / 1e12 if avg_launch_ms > 0 else 0.0
     traffic = kernel_traffic()
-    io_bytes = (q.numel() + k.numel() + v.numel() + o.numel()) * 2 + lse.numel() * 4
+    # Bytes one GPU's step touches: its Q and O rows, all of K and V, the LSE.
+    my_rows = sum(b - a for a, b in my_intervals)
+    io_bytes = (2 * my_rows * w.Hq * w.d + k.numel() + v.numel()) * 2 + lse.numel() * 4
 
     result = None
     if rank == 0:
