@@ -631,7 +631,8 @@ def per_workload_report(args, local):
         lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
         f_ms = timed(lambda: att(q, k, v, o, lse, stream=stream), 2 if big else 5, 1 if big else 3)
         e = {"workload": w.name, "dtype": w.dtype, "schedule": sched_name(w.kind), "P_virtual": w.P,
-             "n_items": int(len(att.items)), "valid_pairs": pairs, "forward_ms": round(f_ms, 4),
+             "n_items": int(len(att.items)), "items_cut_at_documents": True, "valid_pairs": pairs,
+             "forward_ms": round(f_ms, 4),
              "forward_tflops": round(flop / (f_ms * 1e-3) / 1e12, 2),
              "forward_kernel": fwd_kernel_name(w) if w.dtype == "bf16" else f"attn_simt_kernel<{w.d}> (fp32)"}
         if w.dtype == "bf16":
@@ -725,7 +726,8 @@ def balance_report(args, local):
     run alone through sp_packed_attention (one persistent launch on the whole
     GPU), so the slowest rank is the compute critical path of one SP step on P
     GPUs (transfers not included). Packed workloads and the single causal
-    document, with the policies the schedule kind allows."""
+    document, with the policies the schedule kind allows; the packed ones both
+    with the items as built and cut at document boundaries."""
     import torch
     import sequence_blockwise_gb300 as sb
     from sequence_blockwise_gb300 import workloads as wl
@@ -742,7 +744,7 @@ def balance_report(args, local):
         o = torch.empty_like(q)
         lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
         cu_dev = torch.from_numpy(cu).to(dev)
-        for mode in modes:
+        for mode, cut in [(m, c) for m in modes for c in ((False, True) if len(cu) > 2 else (False,))]:
             R = w.P // U
             bounds = None if mode == 0 else sb.sp_chunk_bounds(mode, R, w.T, cu, w.causal)
             if U > 1:
@@ -751,6 +753,8 @@ def balance_report(args, local):
             else:
                 items = sb.sp_schedule_build(kind, w.P, w.T, cu, w.causal, seed=w.seed, bounds=bounds)
                 heads = np.tile(np.array([[0, w.Hq]], dtype=np.int32), (len(items), 1))
+            if cut:
+                items, heads = sb.sp_schedule_split_documents(items, cu, w.causal, heads=heads)
             ms, pairs = [], []
             for r in range(w.P):
                 sel = items[:, 0] == r
@@ -782,7 +786,8 @@ def balance_report(args, local):
             cuts = 0 if bounds is None else int(sum(1 for x in bounds[1:-1] if x not in set(cu.tolist())))
             out.append({"workload": w.name, "schedule": sched_name(kind) + (f" {R}x{U} (head split)" if U > 1 else ""),
                         "P_virtual": w.P,
-                        "chunking": ["equal", "balanced", "balanced_doc"][mode], "n_items": int(len(items)),
+                        "chunking": ["equal", "balanced", "balanced_doc"][mode],
+                        "split_at_documents": cut, "n_items": int(len(items)),
                         "bounds_inside_documents": cuts,
                         "pairs_max_over_mean": round(float(pr_a.max() / pr_a.mean()), 4),
                         "rank_ms_max": round(float(ms_a.max()), 4), "rank_ms_mean": round(float(ms_a.mean()), 4),

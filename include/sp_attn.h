@@ -164,6 +164,34 @@ sp_status sp_schedule_build_hier(sp_sched_kind inter_kind, int32_t R, int32_t U,
                                  uint64_t seed, int32_t Hq, const int32_t* bounds, sp_item* out_items,
                                  int32_t* out_heads, int64_t* inout_n_items);
 
+/* sp_schedule_split_documents — host only; cuts every item of a schedule at
+ * the document boundaries of a packed sequence, so that each output item holds
+ * the (query, key) pairs of one document only ("HSAP: A Hierarchical
+ * Sequence-aware Parallelism for Hybrid-Context Generative Models", abstract:
+ * scheduling of incomplete QKV on hybrid-context packed sequences without
+ * cross-contamination; the per-document cut is this library's reading of that
+ * scheduling at document granularity, not a step the page spells out).
+ *  Item (Q [a,b), KV [c,d)) becomes, for every document D = [s,e) holding a
+ *  valid pair of it, the item (Q [a,b) n D, KV [c,d) n D) with the same rank,
+ *  step and cycle and flags recomputed for the piece (SP_ITEM_DOC_EDGE is then
+ *  never set). The valid pairs covered are exactly the input's.
+ *  Order: each maximal run of consecutive items sharing rank, Q range and (if
+ *  heads is given) head range is replaced by its pieces, document by document
+ *  in token order, each document's pieces in input order. The pieces of one run
+ *  and one document share a Q range, so sp_packed_attention runs every
+ *  document of a rank's chunk as a group of its own: its units walk one
+ *  document's keys, and groups are started longest walk first.
+ *  items: host, n_items items with 0 <= q_begin < q_end <= T and
+ *  0 <= kv_begin < kv_end <= T (T = cu_seqlens_host[ndocs]), else
+ *  SP_ERR_INVALID_ARG. heads: host int32 [n_items][2] query-head ranges
+ *  (sp_schedule_build_hier) or NULL; out_heads receives the pieces' ranges and
+ *  must be given when heads is. cu_seqlens_host as sp_schedule_build (ndocs >=
+ *  1). Two-call protocol of sp_schedule_build for out_items / *inout_n_items.
+ *  Nothing is kept; the inputs are only read. */
+sp_status sp_schedule_split_documents(const sp_item* items, const int32_t* heads, int64_t n_items,
+                                      const int32_t* cu_seqlens_host, int32_t ndocs, int32_t causal,
+                                      sp_item* out_items, int32_t* out_heads, int64_t* inout_n_items);
+
 /* sp_tasp_cycles — host only. Writes the P-1 Hamiltonian cycles that TASP
  * schedules use for (P, seed) as successor tables: out_succ[c * P + u] is the
  * rank after u on ring c. out_succ must hold (P-1)*P int32. P = 1 writes

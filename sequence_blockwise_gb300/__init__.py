@@ -26,7 +26,7 @@ _STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_
            4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_INTERNAL"}
 
 EXPORTED = ["sp_schedule_build", "sp_schedule_build_chunked", "sp_schedule_build_hier", "sp_chunk_bounds",
-            "sp_schedule_link_bytes_hier",
+            "sp_schedule_link_bytes_hier", "sp_schedule_split_documents",
             "sp_tasp_cycles", "sp_packed_attention_ex", "sp_schedule_link_bytes", "sp_partial_attn", "sp_lse_merge",
             "sp_packed_attention_workspace_size", "sp_packed_attention",
             "sp_packed_attention_static_ws", "sp_packed_attention_backward_workspace_size",
@@ -70,6 +70,8 @@ def load():
         lib.sp_schedule_build_hier.restype = ctypes.c_int
         lib.sp_schedule_build_hier.argtypes = [ctypes.c_int, i32, i32, i32, vp, i32, i32, u64, i32, vp, vp,
                                                vp, ctypes.POINTER(ctypes.c_int64)]
+        lib.sp_schedule_split_documents.restype = ctypes.c_int
+        lib.sp_schedule_split_documents.argtypes = [vp, vp, i64, vp, i32, i32, vp, vp, ctypes.POINTER(i64)]
         lib.sp_packed_attention_ex.restype = ctypes.c_int
         lib.sp_packed_attention_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int,
                                                vp, i32, i32, f32, vp, vp, i64, vp, ctypes.c_size_t, vp]
@@ -158,6 +160,33 @@ def sp_schedule_build_hier(inter_kind: int, R: int, U: int, total_tokens: int, c
                                       Hq, bp, items.ctypes.data, heads.ctypes.data, ctypes.byref(cap)),
            "sp_schedule_build_hier")
     return items[:cap.value], heads[:cap.value]
+
+
+def sp_schedule_split_documents(items, cu_seqlens, causal: bool, heads=None):
+    """Every item cut at the document boundaries (one document's pairs per item).
+    Returns items [m, 8], or (items, heads [m, 2]) when head ranges are given."""
+    lib = load()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    it = np.ascontiguousarray(np.asarray(items, dtype=np.int32).reshape(-1, 8))
+    hd = None if heads is None else np.ascontiguousarray(np.asarray(heads, dtype=np.int32).reshape(-1, 2))
+    if hd is not None:
+        _need(len(hd) == len(it), "heads must hold one range per item")
+    if hd is not None and len(hd) == 0:
+        hd = np.zeros((1, 2), dtype=np.int32)  # never read with no items; marks "heads given"
+    ip = it.ctypes.data if len(it) else None
+    hp = None if hd is None else hd.ctypes.data
+    n = ctypes.c_int64(0)
+    _check(lib.sp_schedule_split_documents(ip, hp, len(it), cu.ctypes.data, len(cu) - 1, int(causal), None,
+                                           None, ctypes.byref(n)), "sp_schedule_split_documents")
+    out = np.zeros((max(n.value, 1), 8), dtype=np.int32)
+    out_h = np.zeros((max(n.value, 1), 2), dtype=np.int32)
+    cap = ctypes.c_int64(n.value)
+    _check(lib.sp_schedule_split_documents(ip, hp, len(it), cu.ctypes.data, len(cu) - 1, int(causal),
+                                           out.ctypes.data, out_h.ctypes.data if hd is not None else None,
+                                           ctypes.byref(cap)), "sp_schedule_split_documents")
+    if hd is None:
+        return out[:cap.value]
+    return out[:cap.value], out_h[:cap.value]
 
 
 def sp_schedule_link_bytes_hier(inter_kind: int, R: int, U: int, total_tokens: int, cu_seqlens, causal: bool,
@@ -395,9 +424,13 @@ class PackedAttention:
     sp_packed_attention. Only buffer management lives here."""
 
     def __init__(self, cu_seqlens, causal: bool, kind: int, P: int, Hq: int, seed: int = 0,
-                 device="cuda", chunking: int = SP_CHUNK_EQUAL, ulysses: int = 1):
+                 device="cuda", chunking: int = SP_CHUNK_EQUAL, ulysses: int = 1,
+                 split_documents: bool = True):
         """ulysses > 1: two-level schedule, P / ulysses groups running `kind`
-        between them and a query-head split over `ulysses` ranks inside each."""
+        between them and a query-head split over `ulysses` ranks inside each.
+        split_documents: the schedule's items are cut at document boundaries
+        (sp_schedule_split_documents), so that every document of a rank's chunk
+        runs as a group of its own; False keeps the items as built."""
         torch = _torch()
         self.cu_host = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
         self.T = int(self.cu_host[-1])
@@ -414,6 +447,12 @@ class PackedAttention:
                                                             causal, Hq, seed, bounds=self.bounds)
         else:
             self.items = sp_schedule_build(kind, P, self.T, self.cu_host, causal, seed, bounds=self.bounds)
+        if split_documents:
+            if self.heads is None:
+                self.items = sp_schedule_split_documents(self.items, self.cu_host, causal)
+            else:
+                self.items, self.heads = sp_schedule_split_documents(self.items, self.cu_host, causal,
+                                                                     heads=self.heads)
         self.cu_dev = torch.from_numpy(self.cu_host).to(device)
         self.items_dev = torch.from_numpy(self.items).to(device)
         self.heads_dev = None if self.heads is None else torch.from_numpy(self.heads).to(device)

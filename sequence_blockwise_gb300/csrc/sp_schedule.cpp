@@ -551,6 +551,75 @@ sp_status sp_schedule_build_hier(sp_sched_kind inter_kind, int32_t R, int32_t U,
   return SP_OK;
 }
 
+sp_status sp_schedule_split_documents(const sp_item* items, const int32_t* heads, int64_t n,
+                                      const int32_t* cu, int32_t ndocs, int32_t causal_i,
+                                      sp_item* out, int32_t* out_heads, int64_t* inout_n) {
+  if (!inout_n || n < 0 || (n > 0 && !items) || ndocs < 1 || !cu) return SP_ERR_INVALID_ARG;
+  const int T = cu[ndocs];
+  if (!valid_cu(cu, ndocs, T)) return SP_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    const sp_item& it = items[i];
+    if (it.q_begin < 0 || it.q_begin >= it.q_end || it.q_end > T || it.kv_begin < 0 ||
+        it.kv_begin >= it.kv_end || it.kv_end > T)
+      return SP_ERR_INVALID_ARG;
+  }
+  const bool causal = causal_i != 0;
+  Docs docs{cu, ndocs};
+  // A run is a maximal stretch of items sharing rank, Q range and head range
+  // (one group of sp_packed_attention). Its pieces go out document by
+  // document in token order, each document's pieces in input order.
+  std::vector<sp_item> res;
+  std::vector<int32_t> res_heads;
+  std::vector<std::pair<int, int64_t>> pieces;  // (document, input index)
+  auto same_run = [&](int64_t a, int64_t b) {
+    return items[a].rank == items[b].rank && items[a].q_begin == items[b].q_begin &&
+           items[a].q_end == items[b].q_end &&
+           (!heads || (heads[2 * a] == heads[2 * b] && heads[2 * a + 1] == heads[2 * b + 1]));
+  };
+  for (int64_t r0 = 0; r0 < n;) {
+    int64_t r1 = r0 + 1;
+    while (r1 < n && same_run(r0, r1)) ++r1;
+    pieces.clear();
+    for (int64_t i = r0; i < r1; ++i) {
+      const sp_item& it = items[i];
+      const int d0 = docs.doc_of(std::max(it.q_begin, it.kv_begin));
+      const int d1 = docs.doc_of(std::min(it.q_end, it.kv_end) - 1);
+      for (int d = d0; d <= d1; ++d) pieces.emplace_back(d, i);
+    }
+    std::stable_sort(pieces.begin(), pieces.end(),
+                     [](const std::pair<int, int64_t>& a, const std::pair<int, int64_t>& b) {
+                       return a.first < b.first;
+                     });
+    for (const auto& pc : pieces) {
+      const sp_item& it = items[pc.second];
+      const int ds = cu[pc.first], de = cu[pc.first + 1];
+      const int qa = std::max(it.q_begin, ds), qb = std::min(it.q_end, de);
+      const int ka = std::max(it.kv_begin, ds), kb = std::min(it.kv_end, de);
+      if (!docs.any_valid(qa, qb, ka, kb, causal)) continue;
+      res.push_back(sp_item{it.rank, it.step, it.cycle, qa, qb, ka, kb, docs.flags(qa, qb, ka, kb, causal)});
+      if (heads) {
+        res_heads.push_back(heads[2 * pc.second]);
+        res_heads.push_back(heads[2 * pc.second + 1]);
+      }
+    }
+    r0 = r1;
+  }
+  const int64_t m = static_cast<int64_t>(res.size());
+  if (!out) {
+    *inout_n = m;
+    return SP_OK;
+  }
+  if (heads && !out_heads) return SP_ERR_INVALID_ARG;
+  if (*inout_n < m) {
+    *inout_n = m;
+    return SP_ERR_BUFFER_TOO_SMALL;
+  }
+  if (m) std::memcpy(out, res.data(), sizeof(sp_item) * static_cast<size_t>(m));
+  if (heads && m) std::memcpy(out_heads, res_heads.data(), sizeof(int32_t) * 2 * static_cast<size_t>(m));
+  *inout_n = m;
+  return SP_OK;
+}
+
 }  // extern "C"
 
 extern "C" sp_status sp_schedule_link_bytes(sp_sched_kind kind, int32_t P, int32_t T,

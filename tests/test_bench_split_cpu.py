@@ -1,10 +1,11 @@
 """The benchmark's sequence-parallel split, on CPU with two gloo ranks under
 torchrun: GPU g runs the schedule items of the virtual ranks r with
 r mod N = g. Each rank computes its share of four workloads' schedules (Zigzag,
-TASP, Ring); the test then checks that every schedule item went to exactly one
-rank, that each rank's output rows are exactly the Q chunks its virtual ranks
-own (no row written by two GPUs, none left out), that the FLOP shares add up to
-the workload's, and that the ranks' per-GPU times gather in rank order."""
+TASP, Ring; as built and cut at document boundaries); the test then checks
+that every schedule item went to exactly one rank, that each rank's output
+rows are exactly the Q chunks its virtual ranks own (no row written by two
+GPUs, none left out), that the FLOP shares add up to the workload's, and that
+the ranks' per-GPU times gather in rank order."""
 import json
 import os
 import socket
@@ -55,12 +56,13 @@ def test_split_partitions_items_and_rows_two_gloo_ranks(tmp_path):
         f"for i in {WORKLOADS!r}:\n"
         "    w = wl.WORKLOADS[i]\n"
         "    cu = wl.cu_seqlens(w)\n"
-        "    items = sb.sp_schedule_build(w.kind, w.P, w.T, cu, w.causal, seed=w.seed)\n"
-        "    mine = bench.split_items(items, world, rank)\n"
-        "    res['w'][w.name] = {\n"
-        "        'items': mine.tolist(),\n"
-        "        'rows': bench.row_intervals(mine),\n"
-        "        'pairs': int(sum(bench.valid_pairs_range(cu, w.causal, it) for it in mine))}\n"
+        "    built = sb.sp_schedule_build(w.kind, w.P, w.T, cu, w.causal, seed=w.seed)\n"
+        "    for cut, items in ((0, built), (1, sb.sp_schedule_split_documents(built, cu, w.causal))):\n"
+        "        mine = bench.split_items(items, world, rank)\n"
+        "        res['w'][w.name + str(cut)] = {\n"
+        "            'items': mine.tolist(),\n"
+        "            'rows': bench.row_intervals(mine),\n"
+        "            'pairs': int(sum(bench.valid_pairs_range(cu, w.causal, it) for it in mine))}\n"
         "bench.dist_barrier(world)\n"
         f"open({str(tmp_path)!r} + f'/rank{{rank}}.json', 'w').write(json.dumps(res))\n"
         "torch.distributed.destroy_process_group()\n")
@@ -75,11 +77,14 @@ def test_split_partitions_items_and_rows_two_gloo_ranks(tmp_path):
 
     import bench
     from sequence_blockwise_gb300 import workloads as wl
-    for i in WORKLOADS:
+    for i, cut in [(i, c) for i in WORKLOADS for c in (0, 1)]:
         w = wl.WORKLOADS[i]
         cu = wl.cu_seqlens(w)
         items = sb.sp_schedule_build(w.kind, w.P, w.T, cu, w.causal, seed=w.seed)
-        got = [np.array(r["w"][w.name]["items"], dtype=np.int32).reshape(-1, 8) for r in res]
+        if cut:  # the items as the benchmark runs them: cut at document boundaries
+            items = sb.sp_schedule_split_documents(items, cu, w.causal)
+        key_w = w.name + str(cut)
+        got = [np.array(r["w"][key_w]["items"], dtype=np.int32).reshape(-1, 8) for r in res]
         # Every item exactly once, each on the GPU of its virtual rank.
         both = np.concatenate(got)
         assert len(both) == len(items)
@@ -88,7 +93,7 @@ def test_split_partitions_items_and_rows_two_gloo_ranks(tmp_path):
         for g, mine in enumerate(got):
             assert (mine[:, 0] % 2 == g).all()
         # Each GPU writes exactly the Q chunks its virtual ranks own.
-        rows = [[tuple(x) for x in r["w"][w.name]["rows"]] for r in res]
+        rows = [[tuple(x) for x in r["w"][key_w]["rows"]] for r in res]
         for g in range(2):
             own = _merge([c for vr in range(g, w.P, 2) for c in bench.owned_chunks(w.kind, w.P, w.T, vr)])
             assert rows[g] == own, (w.name, g)
@@ -96,7 +101,7 @@ def test_split_partitions_items_and_rows_two_gloo_ranks(tmp_path):
         assert _merge(rows[0] + rows[1]) == [(0, w.T)]
         assert sum(b - a for a, b in rows[0]) + sum(b - a for a, b in rows[1]) == w.T
         # FLOP shares add up to the workload's.
-        assert sum(r["w"][w.name]["pairs"] for r in res) == bench.valid_pairs(cu, w.causal)
+        assert sum(r["w"][key_w]["pairs"] for r in res) == bench.valid_pairs(cu, w.causal)
 
 
 def test_owned_chunks_and_row_intervals():
