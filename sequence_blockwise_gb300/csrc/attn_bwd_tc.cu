@@ -293,7 +293,7 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, int c0, const uint32_t (&
 // ------------------------------------------------------------------ D_i
 
 // ndsc[h][t] = -scale * (dO[t][h][:] . O[t][h][:]) in fp32 from bf16, and
-// nlse2[h][t] = -lse[h][t] * log2(e); one warp per (t, h). The signs and the
+// nlse2[h][t] = -lse[h][t] * log2(e); d / 8 lanes per (t, h). The signs and the
 // scale are folded in so that the tensor-core kernel needs one FMA per value.
 // Also zeroes the (t, h) row of the fp32 dQ accumulator [T][Hq][d] and the
 // fused kernel's unit counter, which the next kernel on the stream reads, and
@@ -324,29 +324,34 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restr
     }
   }
   const long long n = static_cast<long long>(T) * Hq;
-  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       w < n; w += wstride) {
-    const int t = static_cast<int>(w / Hq), h = static_cast<int>(w % Hq);
-    const uint16_t* po = o + static_cast<size_t>(w) * d;
-    const uint16_t* pd = dout + static_cast<size_t>(w) * d;
-    // 16-byte loads: lane l reads elements [8 l, 8 l + 8) (d = 128: 16 lanes, d = 64: 8).
+  // d / 8 lanes per (t, h) row, each with one 16-byte load of O and of dO
+  // (elements [8 s, 8 s + 8) for sub-lane s), so that a warp takes 256 / d rows
+  // at a time with every lane loading.
+  const int lpr = d >> 3, rpw = 32 / lpr;
+  const int sub = lane / lpr, sl = lane - sub * lpr;
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5) * rpw;
+  for (long long base = (static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * rpw;
+       base < n; base += wstride) {
+    const long long w = base + sub;
+    const bool live = w < n;
     float acc = 0.f;
-    for (int c = 8 * lane; c < d; c += 256) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(po + c));
-      const uint4 b = __ldg(reinterpret_cast<const uint4*>(pd + c));
+    if (live) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + static_cast<size_t>(w) * d) + sl);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + static_cast<size_t>(w) * d) + sl);
       const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc = fmaf(__uint_as_float(av[i] << 16), __uint_as_float(bv[i] << 16), acc);
         acc = fmaf(__uint_as_float(av[i] & 0xffff0000u), __uint_as_float(bv[i] & 0xffff0000u), acc);
       }
+      float4* zq = reinterpret_cast<float4*>(dqacc + static_cast<size_t>(w) * d);
+      zq[2 * sl] = make_float4(0.f, 0.f, 0.f, 0.f);
+      zq[2 * sl + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float4* zq = reinterpret_cast<float4*>(dqacc + static_cast<size_t>(w) * d);
-    for (int c = lane; c < d / 4; c += 32) zq[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
+    // Sum over the row's lanes (xor offsets below lpr stay inside its segment).
+    for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && sl == 0) {
+      const int t = static_cast<int>(w / Hq), h = static_cast<int>(w % Hq);
       const size_t i = static_cast<size_t>(h) * T + t;
       ndsc[i] = -acc * scale;
       nlse2[i] = -lse[i] * LOG2E;
