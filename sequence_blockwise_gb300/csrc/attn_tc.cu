@@ -204,7 +204,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       int armed_q = 0;
       uint32_t par_q = 0;
       bool ok = true;
-      // Work units: claimed from the dynamic queue (largest groups first, so
+      // Work units: claimed from the dynamic queue (longest key walks first, so
       // the tail is made of small units) or strided over the CTAs.
       int k_static = 0;
       auto fetch = [&]() -> int {
