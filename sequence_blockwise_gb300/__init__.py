@@ -475,9 +475,10 @@ class PackedAttention:
         return o, lse
 
     def backward(self, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale=None, stream=None):
-        """Gradients (dq, dk, dv) of the forward call that returned (o, lse)."""
+        """Gradients (dq, dk, dv) of the forward call that returned (o, lse).
+        With a two-level schedule the items of all ranks together cover every
+        head and pair, so the gradients are those of all heads too."""
         torch = _torch()
-        _need(self.heads is None, "the backward takes schedules without a head split")
         T, Hq, d = q.shape
         nbytes = sp_packed_attention_backward_workspace_size(len(self.items), T, Hq)
         if getattr(self, "bwd_workspace", None) is None or self.bwd_workspace.numel() < nbytes:

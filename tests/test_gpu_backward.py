@@ -135,6 +135,26 @@ def test_backward_matches_oracle(case):
         assert fro <= REL_FRO, (name, fro)
 
 
+@pytest.mark.parametrize("inter,R,U", [(sb.SP_SCHED_RING, 2, 2), (sb.SP_SCHED_ZIGZAG, 2, 4)])
+def test_backward_two_level_schedule(inter, R, U):
+    """The backward of a forward run on a two-level schedule (query heads split
+    over the U ranks of each group) against the oracle, same envelope."""
+    T, docs, Hq, Hkv, d = 704, [300, 404], 8, 2, 128
+    cu = wl.cu_from_lengths(docs)
+    q, k, v, do = _inputs(T, Hq, Hkv, d, 19 + U)
+    att = sb.PackedAttention(cu, True, inter, R * U, Hq, ulysses=U)
+    o, lse = att(q, k, v)
+    dq, dk, dv = att.backward(q, k, v, o, lse, do)
+    sb.sp_check_device_status()
+    ref = oracle.attn_backward(host_inputs(q), host_inputs(k), host_inputs(v), host_inputs(do), cu, True)
+    env = _envelopes(q, k, v, do, cu, True, 1.0 / math.sqrt(d))
+    for name, got, r, mm in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, env):
+        g = got.double().cpu().numpy()
+        worst = float(np.max(np.abs(g - r) / (2.0 ** -7 * mm + 2.0 ** -8 * np.abs(r) + 1e-6)))
+        assert worst <= 1.0, (name, worst)
+        assert _rel_fro(g, r) <= REL_FRO, name
+
+
 def test_backward_deterministic_and_schedule_invariant():
     """Two runs give identical dK and dV bits (each is summed in a fixed order)
     and dQ equal up to the rounding of its fp32 reduction order; RING and TASP
