@@ -187,6 +187,8 @@ sp_status sp_schedule_build_hier(sp_sched_kind inter_kind, int32_t R, int32_t U,
  *  (sp_schedule_build_hier) or NULL; out_heads receives the pieces' ranges and
  *  must be given when heads is. cu_seqlens_host as sp_schedule_build (ndocs >=
  *  1). Two-call protocol of sp_schedule_build for out_items / *inout_n_items.
+ *  The cut multiplies the groups by the documents a rank's chunk spans;
+ *  sp_packed_attention takes at most SP_MAX_GROUPS of them.
  *  Nothing is kept; the inputs are only read. */
 sp_status sp_schedule_split_documents(const sp_item* items, const int32_t* heads, int64_t n_items,
                                       const int32_t* cu_seqlens_host, int32_t ndocs, int32_t causal,
@@ -302,9 +304,10 @@ size_t sp_packed_attention_workspace_size(int64_t n_items);
  *  strictly increasing, cu[ndocs] = T); every item lies in [0, T) and holds
  *  at least one (query, key) pair the masks allow under it, as a pruned
  *  schedule built from the same descriptor does (an item without one means
- *  the schedule was built for another packing); the items form at most 8192
- *  groups (runs sharing a rank, Q range and head range) whose Q ranges do
- *  not overlap. */
+ *  the schedule was built for another packing); the items form at most
+ *  SP_MAX_GROUPS groups (runs sharing a rank, Q range and head range) whose Q
+ *  ranges do not overlap. */
+#define SP_MAX_GROUPS 8192
 sp_status sp_packed_attention(const void* q, const void* k, const void* v, void* o, float* lse,
                               int32_t T, int32_t Hq, int32_t Hkv, int32_t d, sp_dtype dtype,
                               const int32_t* cu_seqlens_dev, int32_t ndocs, int32_t causal, float scale,

@@ -206,6 +206,19 @@ def sp_schedule_link_bytes_hier(inter_kind: int, R: int, U: int, total_tokens: i
 
 
 SP_CHUNK_EQUAL, SP_CHUNK_BALANCED, SP_CHUNK_BALANCED_DOC = 0, 1, 2
+SP_MAX_GROUPS = 8192  # include/sp_attn.h: groups sp_packed_attention takes
+
+
+def n_groups(items, heads=None) -> int:
+    """Groups of an item list as sp_packed_attention forms them: maximal runs
+    of consecutive items sharing rank, Q range and (if given) head range."""
+    it = np.asarray(items).reshape(-1, 8)
+    if len(it) == 0:
+        return 0
+    key = it[:, [0, 3, 4]]
+    if heads is not None:
+        key = np.concatenate([key, np.asarray(heads).reshape(-1, 2)], axis=1)
+    return int(1 + np.count_nonzero((key[1:] != key[:-1]).any(axis=1)))
 
 
 def sp_chunk_bounds(mode: int, P: int, total_tokens: int, cu_seqlens, causal: bool) -> np.ndarray:
@@ -430,7 +443,9 @@ class PackedAttention:
         between them and a query-head split over `ulysses` ranks inside each.
         split_documents: the schedule's items are cut at document boundaries
         (sp_schedule_split_documents), so that every document of a rank's chunk
-        runs as a group of its own; False keeps the items as built."""
+        runs as a group of its own, unless that would make more than
+        SP_MAX_GROUPS groups (`documents_cut` tells which); False keeps the
+        items as built."""
         torch = _torch()
         self.cu_host = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
         self.T = int(self.cu_host[-1])
@@ -447,12 +462,16 @@ class PackedAttention:
                                                             causal, Hq, seed, bounds=self.bounds)
         else:
             self.items = sp_schedule_build(kind, P, self.T, self.cu_host, causal, seed, bounds=self.bounds)
+        self.documents_cut = False
         if split_documents:
             if self.heads is None:
-                self.items = sp_schedule_split_documents(self.items, self.cu_host, causal)
+                cut, cut_heads = sp_schedule_split_documents(self.items, self.cu_host, causal), None
             else:
-                self.items, self.heads = sp_schedule_split_documents(self.items, self.cu_host, causal,
-                                                                     heads=self.heads)
+                cut, cut_heads = sp_schedule_split_documents(self.items, self.cu_host, causal, heads=self.heads)
+            # A packing of very many documents keeps the items as built when the
+            # cut would pass the group limit of sp_packed_attention.
+            if n_groups(cut, cut_heads) <= SP_MAX_GROUPS:
+                self.items, self.heads, self.documents_cut = cut, cut_heads, True
         self.cu_dev = torch.from_numpy(self.cu_host).to(device)
         self.items_dev = torch.from_numpy(self.items).to(device)
         self.heads_dev = None if self.heads is None else torch.from_numpy(self.heads).to(device)

@@ -57,7 +57,7 @@ __device__ bool item_has_pair(const int32_t* cu, int nd, int qb, int qe, int kb,
 
 // Largest number of groups the set-up kernel orders and checks for overlap
 // (the checks are quadratic in the group count); longer lists are rejected.
-constexpr int MAX_GROUPS = 8192;
+constexpr int MAX_GROUPS = SP_MAX_GROUPS;
 
 __global__ void __launch_bounds__(1024)
 prep_kernel(const sp_item* __restrict__ items, const int32_t* __restrict__ heads, int n, int T, int Hq,

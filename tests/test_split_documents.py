@@ -174,3 +174,24 @@ def test_argument_errors():
     e, eh = sb.sp_schedule_split_documents(np.zeros((0, 8), dtype=np.int32), cu, True,
                                            heads=np.zeros((0, 2), dtype=np.int32))
     assert len(e) == 0 and len(eh) == 0
+
+
+def test_group_limit_and_fallback():
+    """sp_packed_attention takes at most SP_MAX_GROUPS groups; PackedAttention
+    keeps the items as built when cutting them would pass that."""
+    import os
+    import re
+    header = os.path.join(os.path.dirname(__file__), "..", "include", "sp_attn.h")
+    assert int(re.search(r"#define SP_MAX_GROUPS (\d+)", open(header).read()).group(1)) == sb.SP_MAX_GROUPS
+    items = np.array([[0, 0, 0, 0, 4, 0, 4, 0], [0, 1, 0, 0, 4, 4, 8, 0], [1, 0, 0, 4, 8, 4, 8, 0],
+                      [0, 2, 0, 0, 4, 8, 9, 0]], dtype=np.int32)
+    assert sb.n_groups(items) == 3 and sb.n_groups(items[:0]) == 0
+    assert sb.n_groups(items, np.array([[0, 2], [2, 4], [0, 2], [0, 2]])) == 4
+    few = wl.cu_from_lengths([300, 212])
+    att = sb.PackedAttention(few, True, sb.SP_SCHED_RING, 2, 4, device="cpu")
+    assert att.documents_cut and sb.n_groups(att.items) == 3
+    many = wl.cu_from_lengths([8] * 10000)  # 10,000 documents: 10,000 groups once cut
+    att = sb.PackedAttention(many, True, sb.SP_SCHED_RING, 2, 4, device="cpu")
+    assert not att.documents_cut
+    assert np.array_equal(att.items, sb.sp_schedule_build(sb.SP_SCHED_RING, 2, 80000, many, True))
+    assert sb.n_groups(sb.sp_schedule_split_documents(att.items, many, True)) > sb.SP_MAX_GROUPS
