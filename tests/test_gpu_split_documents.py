@@ -123,3 +123,23 @@ def test_cut_512k_balanced_full_size_long_walks():
     eo, el = max_errs(o[rt].float().cpu().numpy().astype(np.float64),
                       lse[:, rt].t().cpu().numpy().astype(np.float64), o_ref, l_ref)
     assert eo <= TOL_BF16_O and el <= TOL_BF16_LSE, (eo, el)
+
+
+@pytest.mark.parametrize("ndocs,kind,P,causal", [(2000, sb.SP_SCHED_TASP, 5, True),
+                                                 (2000, sb.SP_SCHED_RING, 4, False),
+                                                 (9000, sb.SP_SCHED_RING, 2, True)],
+                         ids=["2000docs-tasp5", "2000docs-ring4-full", "9000docs-ring2-uncut"])
+def test_many_short_documents(ndocs, kind, P, causal):
+    """Thousands of 1-20-token documents, every row against the oracle: cut at
+    documents (2,000) and, above the group limit, as built (9,000)."""
+    rng = np.random.default_rng(ndocs + P)
+    lens = rng.integers(1, 21, size=ndocs)
+    cu = wl.cu_from_lengths(lens.tolist())
+    T, Hq, Hkv = int(cu[-1]), 4, 2
+    q, k, v = _inputs(T, Hq, Hkv, 90 + P)
+    att = sb.PackedAttention(cu, causal, kind, P, Hq, seed=1)
+    assert att.documents_cut == (ndocs == 2000)
+    o, lse = att(q, k, v)
+    sb.sp_check_device_status()
+    eo, el = _vs_oracle(q, k, v, cu, causal, o, lse)
+    assert eo <= TOL_BF16_O and el <= TOL_BF16_LSE, (eo, el)
