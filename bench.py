@@ -594,7 +594,8 @@ def run_ours(args, world, rank, local):
 def per_workload_report(args, local):
     """Forward time of every workload on this GPU (and the backward's for the
     bf16 ones), each workload's full schedule in one sp_packed_attention call,
-    CUDA events around each call, median over the calls. For the 64K full-mask
+    timed over calls issued back to back between two CUDA events (per-call
+    average, median of a few such runs). For the 64K full-mask
     layer also the API path: one sp_partial_attn per schedule item into fp32
     partials and an sp_lse_merge per further item of a Q range."""
     import torch
@@ -604,18 +605,23 @@ def per_workload_report(args, local):
     stream = torch.cuda.current_stream(dev)
     peak = read_peaks()["bf16_tflops"]
 
-    def timed(fn, n, warm):
+    def timed(fn, n, warm, reps=3):
+        # n calls back to back between two events, so that the launches queue
+        # on the stream and the host's argument marshalling between calls does
+        # not leave the GPU idle inside the timed region; per-call average,
+        # median over `reps` such runs.
         for _ in range(warm):
             fn()
         torch.cuda.synchronize(dev)
         ts = []
-        for _ in range(n):
+        for _ in range(reps):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            fn()
+            for _ in range(n):
+                fn()
             b.record(stream)
             torch.cuda.synchronize(dev)
-            ts.append(a.elapsed_time(b))
+            ts.append(a.elapsed_time(b) / n)
         sb.sp_check_device_status(stream)
         return float(np.median(ts))
 
@@ -629,7 +635,9 @@ def per_workload_report(args, local):
         att = sb.PackedAttention(cu, w.causal, w.kind, w.P, w.Hq, seed=w.seed, device=dev)
         o = torch.empty_like(q)
         lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
-        f_ms = timed(lambda: att(q, k, v, o, lse, stream=stream), 2 if big else 5, 1 if big else 3)
+        sampler = ClockSampler(local)  # clocks while this workload's calls run
+        f_ms = timed(lambda: att(q, k, v, o, lse, stream=stream), 2 if big else 5, 1 if big else 3,
+                     reps=2 if big else 3)
         e = {"workload": w.name, "dtype": w.dtype, "schedule": sched_name(w.kind), "P_virtual": w.P,
              "n_items": int(len(att.items)), "items_cut_at_documents": True, "valid_pairs": pairs,
              "forward_ms": round(f_ms, 4),
@@ -641,7 +649,7 @@ def per_workload_report(args, local):
             dout = wl.random_normal((w.T, w.Hq, w.d), w.seed + 99, dev, "bf16")
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
             b_ms = timed(lambda: att.backward(q, k, v, o, lse, dout, dq, dk, dv, stream=stream),
-                         1 if big else 3, 1 if big else 2)
+                         1 if big else 3, 1 if big else 2, reps=2 if big else 3)
             e["backward_ms"] = round(b_ms, 4)
             e["backward_tflops"] = round(2.5 * flop / (b_ms * 1e-3) / 1e12, 2)
             e["backward_frac_of_peak"] = round(2.5 * flop / (b_ms * 1e-3) / 1e12 / peak, 4)
@@ -675,6 +683,7 @@ def per_workload_report(args, local):
                              "what": "one sp_partial_attn per item (fp32 partials) + sp_lse_merge per "
                                      "further item of a Q range"}
             del acc, accl
+        e["clocks"] = sampler.stop()
         out.append(e)
         del q, k, v, o, lse, att
         torch.cuda.empty_cache()
