@@ -46,9 +46,10 @@ constexpr int REC_TILE = 16, REC_LAST = 32;
 struct PCfg {
   static constexpr int D = 128;
   // Two Q buffers (the next unit's Q tiles load while the current unit runs),
-  // two K and three V stages (V is held one MMA group longer than K).
+  // three K and three V stages (V is held one MMA group longer than K): copies
+  // run two tiles ahead (with two K stages, one: 0.3-0.6% slower).
   static constexpr int QBUF = 2;
-  static constexpr int KSTAGE = 2;
+  static constexpr int KSTAGE = 3;
   static constexpr int VSTAGE = 3;
   static constexpr int Q_SUB = 128 * 128;           // [128 rows][64 dims] bf16
   static constexpr int Q_TILE = 2 * Q_SUB;          // 128 rows x 128 dims
@@ -64,7 +65,7 @@ struct PCfg {
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;   // TMEM address, abort flag
   static constexpr int OFF_REC = OFF_MISC + 8;
   static constexpr int OFF_URING = (OFF_REC + 4 * KSTAGE + 15) & ~15;  // two unit records
-  static constexpr int SMEM_ALLOC = OFF_URING + 2 * 128 + 1024;
+  static constexpr int SMEM_ALLOC = OFF_URING + 2 * 128 + 1024;  // 230,880 of 232,448 bytes
   static constexpr int TM_S = 0;
   static constexpr int TM_O = 256;
   static constexpr int TMEM_COLS = 512;
@@ -79,10 +80,11 @@ struct PCfg {
 // used in the first CTA only; the others exist in both CTAs and receive the
 // MMA lane's multicast commits. Q_FULL / Q_EMPTY: one per Q buffer.
 enum {
-  B_Q_FULL = 0, B_Q_EMPTY = 2, B_KV_FULL = 4, B_K_EMPTY = 6, B_V_EMPTY = 8,
-  B_S_FULL = 12, B_P_FULL = 14, B_O_FULL = 16, B_DRAIN = 18, B_U_FULL = 19, B_U_EMPTY = 21
+  B_Q_FULL = 0, B_Q_EMPTY = 2, B_KV_FULL = 4, B_K_EMPTY = 7, B_V_EMPTY = 10,
+  B_S_FULL = 13, B_P_FULL = 15, B_O_FULL = 17, B_DRAIN = 19, B_U_FULL = 20, B_U_EMPTY = 22
 };
 static_assert(B_U_EMPTY + 2 <= PCfg::N_BARS, "barrier slots");
+static_assert(PCfg::SMEM_ALLOC <= 232448, "pair kernel layout exceeds the shared memory of a block");
 
 // A unit slot holds the unit's record (sp_tiles.cuh), built by the first CTA's
 // scheduler warp and stored into both CTAs' slot. Both CTAs' units have the
