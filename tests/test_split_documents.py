@@ -148,6 +148,11 @@ def test_workload_splits():
             off = 1 if col in (4, 6) else 0
             assert np.array_equal(np.searchsorted(cu, split[:, col] - off, side="right"), d0)
         _check_order(split)
+        # Every piece is its parent intersected with one document, so the pieces
+        # cover each valid pair exactly once when the parents do (the schedule
+        # tests check that), and no (parent, document) with a valid pair is lost:
+        # the valid pairs add up to the workload's (above).
+        _check_pieces(items, split, cu, w.causal)
 
 
 def test_argument_errors():
