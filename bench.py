@@ -481,6 +481,12 @@ def run_ours(args, world, rank, local):
         for _ in range(max(args.warmup, 3)):
             bstep()
         torch.cuda.synchronize(dev)
+        # The timed backward starts, like the headline's forward region, from a
+        # GPU that has idled for a moment (the end-to-end region just before it
+        # ran at the power cap), and its clocks are recorded beside it.
+        time.sleep(1.0)
+        bclocks = ClockSampler(local)
+        time.sleep(0.3)
         bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         for i in range(args.steps):
@@ -488,6 +494,7 @@ def run_ours(args, world, rank, local):
             bstep()
             bev[i][1].record(stream)
         torch.cuda.synchronize(dev)
+        bclk = bclocks.stop()
         sb.sp_check_device_status(stream)
         bper = [a.elapsed_time(b) for a, b in bev]
         b_ms = dist_max(sum(bper) / len(bper), world)
@@ -495,7 +502,8 @@ def run_ours(args, world, rank, local):
         bwd = {"ms_per_call": round(b_ms, 4), "tflops": round(bflop / (b_ms * 1e-3) / 1e12, 2),
                "flop_per_call": bflop, "flop_convention": "10*d*Hq*valid_pairs (2.5x forward)",
                "frac_of_peak": None, "launches_per_call": 3,
-               "kernels": "bwd_rowdot_kernel, bwd_fused_kernel<128>, bwd_dq_convert_kernel"}
+               "kernels": "bwd_rowdot_kernel, bwd_fused_kernel<128>, bwd_dq_convert_kernel",
+               "clocks": bclk}
         del dout, dq, dk, dv
 
     # ---- secondary: the log-sum-exp merge kernel of the unfused API path,
