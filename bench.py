@@ -621,6 +621,7 @@ def per_workload_report(args, local):
         for _ in range(warm):
             fn()
         torch.cuda.synchronize(dev)
+        time.sleep(1.0)  # each timed region starts from an idle GPU, as the headline's does
         ts = []
         for _ in range(reps):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
